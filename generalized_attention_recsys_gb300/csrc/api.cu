@@ -1,0 +1,357 @@
+// C ABI of libgdpa.so: argument checks, tensor maps, work lists, launches.
+//
+// The entry points follow the flash_attn_varlen_func statement of the
+// problem on the gdpa/README.md page ("CUTE-DSL" API block): packed q/k/v with
+// cumulative sequence offsets, max lengths, an activation, scale, causal flag
+// and window. See include/gdpa.h for argument meaning and error behaviour.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/gdpa.h"
+#include "args.h"
+#include "common.cuh"
+
+namespace gdpa {
+
+// Per-device status word written by kernels whose bounded waits gave up.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  static int* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  static int counts[kMaxDevices] = {};
+  if (counts[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [rows, heads, dim] row-major tensor as a 3-D map (dim, heads, rows) with
+// a (128-byte, 1, 128-row) box and 128-byte swizzle. rows == 0 is encoded as
+// one row over `fallback` (the kernels never read it then).
+bool make_map(CUtensorMap* m, const void* ptr, int rows, int heads, int dim, int dtype, const void* fallback) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int esz = dtype == DT_E4M3 ? 1 : 2;
+  const CUtensorMapDataType dt = dtype == DT_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == DT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (rows <= 0 || ptr == nullptr) {
+    rows = 1;
+    ptr = fallback;
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * esz, static_cast<cuuint64_t>(heads) * dim * esz};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Upper bounds on work-list entries: sum over sequences of ceil(L / rows).
+size_t fwd_list_cap(const gdpa_shape* s) {
+  return static_cast<size_t>(s->total_q) / kFwdItemRows + static_cast<size_t>(s->batch) + 1;
+}
+size_t bwd_list_cap(const gdpa_shape* s) {
+  return static_cast<size_t>(s->total_k) / kTileK + static_cast<size_t>(s->batch) + 1;
+}
+size_t list_bytes(size_t cap) { return round256(16 + 8 * cap); }
+
+int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int window) {
+  (void)causal;
+  (void)window;
+  if (!s) return GDPA_ERR_INVALID;
+  if (s->batch < 0 || s->total_q < 0 || s->total_k < 0 || max_q < 0 || max_k < 0) return GDPA_ERR_INVALID;
+  if (s->h_q <= 0 || s->h_kv <= 0 || s->h_q % s->h_kv != 0) return GDPA_ERR_INVALID;
+  if (s->dtype < GDPA_BF16 || s->dtype > GDPA_E4M3) return GDPA_ERR_INVALID;
+  if (act < GDPA_ACT_IDENTITY || act > GDPA_ACT_SOFTMAX) return GDPA_ERR_INVALID;
+  const bool ok_dims = (s->d_qk == 64 && s->d_v == 64) || (s->d_qk == 96 && s->d_v == 96) ||
+                       (s->d_qk == 128 && s->d_v == 128) || (s->d_qk == 192 && s->d_v == 128);
+  if (!ok_dims) return GDPA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(s->total_q) * s->h_q * (s->d_qk > s->d_v ? s->d_qk : s->d_v) >= (1ll << 40))
+    return GDPA_ERR_UNSUPPORTED;
+  return GDPA_OK;
+}
+
+// Work list: entries (b, blk) sorted by cost, heaviest first (counting sort
+// over cost buckets). mode 0: blk = 256-row query item, cost = KV blocks it
+// visits; mode 1: blk = 128-row key block, cost = query blocks that see it.
+constexpr int kBuckets = 2048;
+
+__device__ __forceinline__ int item_cost(const Problem& pb, int mode, int b, int blk, int lq, int lk) {
+  int lo, hi;
+  if (mode == 0) {
+    const int r0 = blk * kFwdItemRows;
+    const int r1 = min(lq, r0 + kFwdItemRows) - 1;
+    if (!key_range(r0, r1, lq, lk, pb.causal, pb.window, lo, hi)) return 0;
+    return hi / kTileK - lo / kTileK + 1;
+  }
+  const int k0 = blk * kTileK;
+  const int k1 = min(lk, k0 + kTileK) - 1;
+  if (!query_range(k0, k1, lq, lk, pb.causal, pb.window, lo, hi)) return 0;
+  return hi / kTileQ - lo / kTileQ + 1;
+}
+
+__global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, WorkList* wl, int cap) {
+  __shared__ int hist[kBuckets];
+  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int rows = mode == 0 ? kFwdItemRows : kTileK;
+  for (int b = threadIdx.x; b < pb.batch; b += blockDim.x) {
+    int qs, lq, ks, lk;
+    seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
+    seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
+    const int len = mode == 0 ? lq : lk;
+    const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int c = min(item_cost(pb, mode, b, blk, lq, lk), kBuckets - 1);
+      atomicAdd(&hist[c], 1);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int c = kBuckets - 1; c >= 0; --c) {
+      const int t = hist[c];
+      hist[c] = run;
+      run += t;
+    }
+    wl->count = run < cap ? run : cap;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < pb.batch; b += blockDim.x) {
+    int qs, lq, ks, lk;
+    seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
+    seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
+    const int len = mode == 0 ? lq : lk;
+    const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int c = min(item_cost(pb, mode, b, blk, lq, lk), kBuckets - 1);
+      const int p = atomicAdd(&hist[c], 1);
+      if (p < cap) wl->items[p] = make_int2(b, blk);
+    }
+  }
+}
+
+Problem make_problem(const gdpa_shape* s, const int32_t* cu_q, const int32_t* cu_k, int max_q, int max_k,
+                     int causal, int window) {
+  Problem pb;
+  pb.batch = s->batch;
+  pb.total_q = s->total_q;
+  pb.total_k = s->total_k;
+  pb.h_q = s->h_q;
+  pb.h_kv = s->h_kv;
+  pb.group = s->h_q / s->h_kv;
+  pb.max_q = max_q;
+  pb.max_k = max_k;
+  pb.cu_q = cu_q;
+  pb.cu_k = cu_k;
+  pb.causal = causal ? 1 : 0;
+  pb.window = window > 0 ? window : 0;
+  return pb;
+}
+
+}  // namespace
+}  // namespace gdpa
+
+using namespace gdpa;
+
+extern "C" {
+
+size_t gdpa_workspace_bytes(const gdpa_shape* s, int max_q, int max_k, int is_bwd) {
+  if (validate(s, max_q, max_k, GDPA_ACT_IDENTITY, 0, 0) != GDPA_OK) return 0;
+  if (!is_bwd) return list_bytes(fwd_list_cap(s));
+  size_t b = list_bytes(bwd_list_cap(s));
+  b += round256(static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float));  // dQ accumulator
+  b += round256(static_cast<size_t>(s->total_q) * s->h_q * sizeof(float));            // softmax rowsum(dO*O)
+  return b;
+}
+
+int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, const int32_t* cu_q,
+             const int32_t* cu_k, int max_q, int max_k, int act, float scale, int causal, int window,
+             const float* descale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+             void* stream_) {
+  int st = validate(s, max_q, max_k, act, causal, window);
+  if (st != GDPA_OK) return st;
+  if (s->total_q == 0 || s->batch == 0) return GDPA_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return GDPA_ERR_INVALID;
+  if (s->total_k > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return GDPA_ERR_INVALID;
+  if ((cu_q == nullptr) != (cu_k == nullptr)) return GDPA_ERR_INVALID;
+  if (!cu_q && (s->total_q != s->batch * max_q || s->total_k != s->batch * max_k)) return GDPA_ERR_INVALID;
+  if (act == GDPA_ACT_SOFTMAX && !lse) return GDPA_ERR_INVALID;
+  if (s->dtype == GDPA_E4M3 && !descale) return GDPA_ERR_INVALID;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, 0))
+    return GDPA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const int nsm = sm_count();
+  int* status = status_ptr();
+  if (nsm <= 0 || !status) return GDPA_ERR_CUDA;
+
+  const Problem pb = make_problem(s, cu_q, cu_k, max_q, max_k, causal, window);
+  WorkList* wl = static_cast<WorkList*>(workspace);
+  const int cap = static_cast<int>(fwd_list_cap(s));
+  build_worklist<<<1, 1024, 0, stream>>>(pb, 0, wl, cap);
+  if (cudaGetLastError() != cudaSuccess) return GDPA_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, s->total_q, s->h_q, s->d_qk, s->dtype, workspace) ||
+      !make_map(&tk, k, s->total_k, s->h_kv, s->d_qk, s->dtype, workspace) ||
+      !make_map(&tv, v, s->total_k, s->h_kv, s->d_v, s->dtype, workspace))
+    return GDPA_ERR_CUDA;
+
+  FwdArgs a;
+  a.pb = pb;
+  a.act = act;
+  a.scale = scale;
+  a.descale = descale;
+  a.out = out;
+  a.lse = lse;
+  a.work = wl;
+  a.status = status;
+  cudaError_t e;
+  switch (s->d_qk) {
+    case 64: e = launch_fwd_d64(s->dtype, tq, tk, tv, a, nsm, stream); break;
+    case 96: e = launch_fwd_d96(s->dtype, tq, tk, tv, a, nsm, stream); break;
+    case 128: e = launch_fwd_d128(s->dtype, tq, tk, tv, a, nsm, stream); break;
+    default: e = launch_fwd_d192(s->dtype, tq, tk, tv, a, nsm, stream); break;
+  }
+  return e == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, const int32_t* cu_q,
+             const int32_t* cu_k, int max_q, int max_k, int act, float scale, int causal, int window,
+             const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream_) {
+  int st = validate(s, max_q, max_k, act, causal, window);
+  if (st != GDPA_OK) return st;
+  if (s->dtype == GDPA_E4M3) return GDPA_ERR_UNSUPPORTED;
+  if (deterministic) return GDPA_ERR_UNSUPPORTED;
+  if (s->batch == 0 || (s->total_q == 0 && s->total_k == 0)) return GDPA_OK;
+  if ((cu_q == nullptr) != (cu_k == nullptr)) return GDPA_ERR_INVALID;
+  if (!cu_q && (s->total_q != s->batch * max_q || s->total_k != s->batch * max_k)) return GDPA_ERR_INVALID;
+  const void* need[] = {q, dout, dq};
+  for (const void* p : need)
+    if (s->total_q > 0 && (!p || !aligned16(p))) return GDPA_ERR_INVALID;
+  const void* need_k[] = {k, v, dk, dv};
+  for (const void* p : need_k)
+    if (s->total_k > 0 && (!p || !aligned16(p))) return GDPA_ERR_INVALID;
+  if (act == GDPA_ACT_SOFTMAX && (!out || !lse || !aligned16(out))) return GDPA_ERR_INVALID;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, 1))
+    return GDPA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const int nsm = sm_count();
+  int* status = status_ptr();
+  if (nsm <= 0 || !status) return GDPA_ERR_CUDA;
+
+  const Problem pb = make_problem(s, cu_q, cu_k, max_q, max_k, causal, window);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int cap = static_cast<int>(bwd_list_cap(s));
+  WorkList* wl = reinterpret_cast<WorkList*>(ws);
+  ws += list_bytes(cap);
+  float* dq_acc = reinterpret_cast<float*>(ws);
+  ws += round256(static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float));
+  float* drow = reinterpret_cast<float*>(ws);
+
+  build_worklist<<<1, 1024, 0, stream>>>(pb, 1, wl, cap);
+  if (cudaGetLastError() != cudaSuccess) return GDPA_ERR_CUDA;
+
+  BwdArgs a;
+  a.pb = pb;
+  a.act = act;
+  a.scale = scale;
+  a.work = wl;
+  a.status = status;
+  a.out = out;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = dq_acc;
+  a.drow = drow;
+  a.d_qk = s->d_qk;
+  a.d_v = s->d_v;
+  a.dtype = s->dtype;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, s->total_q, s->h_q, s->d_qk, s->dtype, workspace) ||
+      !make_map(&tk, k, s->total_k, s->h_kv, s->d_qk, s->dtype, workspace) ||
+      !make_map(&tv, v, s->total_k, s->h_kv, s->d_v, s->dtype, workspace) ||
+      !make_map(&tdo, dout, s->total_q, s->h_q, s->d_v, s->dtype, workspace))
+    return GDPA_ERR_CUDA;
+  const cudaError_t e = launch_bwd(tq, tk, tv, tdo, a, nsm, stream);
+  return e == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+int gdpa_get_status(void* stream_) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream_)) != cudaSuccess) return GDPA_ERR_CUDA;
+  int* p = status_ptr();
+  if (!p) return GDPA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return GDPA_ERR_CUDA;
+  }
+  return v;
+}
+
+const char* gdpa_error_string(int s) {
+  switch (s) {
+    case GDPA_OK: return "ok";
+    case GDPA_ERR_INVALID: return "invalid argument";
+    case GDPA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GDPA_ERR_CUDA: return "CUDA error";
+    case GDPA_ERR_WORKSPACE: return "workspace missing or too small";
+    case GDPA_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int gdpa_num_sms(void) { return sm_count(); }
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Kernel argument blocks and the launchers each instantiation unit exports.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gdpa {
+
+struct FwdArgs {
+  Problem pb;
+  int act;
+  float scale;
+  const float* descale;  // e4m3: (q, k, v) per-tensor scales; else NULL
+  void* out;             // [total_q, h_q, dv]; bf16 for bf16/e4m3 inputs, f16 for f16
+  float* lse;            // [h_q, total_q] (softmax)
+  const WorkList* work;
+  int* status;  // device status word; a bounded wait that gave up writes 5 (timeout)
+};
+
+struct BwdArgs {
+  Problem pb;
+  int act;
+  float scale;
+  const WorkList* work;
+  int* status;
+  const void* out;   // softmax: forward output [total_q, h_q, dv]
+  const float* lse;  // softmax: [h_q, total_q]
+  const void* dout;  // [total_q, h_q, dv]
+  void* dq;          // [total_q, h_q, dqk]
+  void* dk;          // [total_k, h_kv, dqk]
+  void* dv;          // [total_k, h_kv, dv]
+  float* dq_acc;     // workspace: fp32 [total_q, h_q, dqk]
+  float* drow;       // workspace: softmax rowsum(dO * O), [h_q, total_q]
+  int d_qk, d_v, dtype;
+};
+
+cudaError_t launch_fwd_d64(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const FwdArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_d96(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const FwdArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_d128(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_d192(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& a, int grid, cudaStream_t stream);
+
+// Backward: dQ accumulator clear, (softmax) rowsum(dO * O), the main
+// kernel, and the dQ conversion, all on `stream`.
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+
+}  // namespace gdpa

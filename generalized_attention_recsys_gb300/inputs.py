@@ -97,6 +97,7 @@ class Inputs:
     v: torch.Tensor
     dout: torch.Tensor | None        # bf16/fp16 [Tq, Hq, dv] (None when forward only)
     descale: tuple[float, float, float] | None = None   # e4m3: per-tensor scales of q, k, v
+    fixed_length: bool = False       # every sequence has max_q / max_k tokens (no cu_seqlens)
 
     @property
     def total_q(self) -> int:
@@ -123,7 +124,7 @@ class Inputs:
         return t.double()
 
     def is_fixed_length(self) -> bool:
-        return self.wl.jagged_q is None and self.wl.jagged_k is None and not self.wl.k_follows_q
+        return self.fixed_length
 
 
 def _cu(lengths: torch.Tensor) -> torch.Tensor:
@@ -182,7 +183,8 @@ def make_inputs(wl: Workload, seed: int = 0, with_dout: bool | None = None) -> I
         q, k, v = _cast(q, wl.dtype), _cast(k, wl.dtype), _cast(v, wl.dtype)
         if dout is not None:
             dout = _cast(dout, wl.dtype)
-    return Inputs(wl, lq, lk, cu_q, cu_k, q, k, v, dout, descale)
+    fixed = wl.jagged_q is None and wl.jagged_k is None and not wl.k_follows_q
+    return Inputs(wl, lq, lk, cu_q, cu_k, q, k, v, dout, descale, fixed)
 
 
 def custom(batch: int, h_q: int, h_kv: int, d_qk: int, d_v: int, lengths_q, lengths_k,

@@ -1,0 +1,149 @@
+/*
+ * gdpa.h -- C ABI of libgdpa.so: Generalized Dot Product Attention (GDPA)
+ * forward and backward on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (gdpa/README.md of facebookresearch/ads_model_kernel_library,
+ * intro paragraph and "Features"): for every sequence b and query head h, with
+ * kv head g = h / (h_q / h_kv),
+ *
+ *     Z = scale * Q_bh K_bg^T,   P = where(M, act(Z), 0),   O = P V_bg
+ *
+ * M is the causal / sliding-window / length mask; masked and out-of-length
+ * positions contribute exactly zero and there is no row normalisation. The
+ * backward (same page, "Features": forward and backward kernels) returns
+ *
+ *     dV_bg += P^T dO,  dS = scale * where(M, (dO V_bg^T) * act'(Z), 0),
+ *     dQ_bh = dS K_bg,  dK_bg += dS^T Q_bh.
+ *
+ * GDPA_ACT_SOFTMAX selects ordinary softmax attention (online softmax with a
+ * log-sum-exp per row, as in the Dao-AILab/flash-attention overview) for
+ * cross-checking.
+ *
+ * The argument list follows the page's "CUTE-DSL" API block,
+ * flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+ * max_seqlen_k, activation=...): packed (jagged) tensors plus cumulative
+ * sequence offsets.
+ *
+ * Layouts. q [total_q, h_q, d_qk], k [total_k, h_kv, d_qk],
+ * v [total_k, h_kv, d_v], out/dout [total_q, h_q, d_v], all row-major with the
+ * head dimension contiguous (element strides h*d, d, 1). cu_seqlens_q/k are
+ * int32 [batch+1] device arrays, non-decreasing, cu[0] = 0, cu[batch] = total;
+ * NULL means every sequence has max_seqlen tokens (the fixed-length
+ * [batch, seq, heads, dim] layout of flash_attn_func, the same memory).
+ * lse is float [h_q, total_q].
+ *
+ * Ownership. The caller allocates every buffer, including the workspace, whose
+ * size gdpa_workspace_bytes() returns. The library allocates no device memory
+ * and keeps no per-call state. Calls are asynchronous on `stream` (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream).
+ *
+ * Errors. Problems visible on the host are returned before any launch:
+ * GDPA_ERR_INVALID (null or misaligned pointer, negative size, h_q % h_kv,
+ * bad enum), GDPA_ERR_UNSUPPORTED (head dims other than (64,64), (96,96),
+ * (128,128), (192,128); FP8 backward), GDPA_ERR_WORKSPACE (too small),
+ * GDPA_ERR_CUDA (a launch or tensor-map encode failed). Every device-side wait
+ * is bounded; a wait that gives up records GDPA_ERR_TIMEOUT in a per-device
+ * status word that gdpa_get_status() returns. cu_seqlens consistency
+ * (monotone, lengths <= max_seqlen, cu[batch] = total) is a caller
+ * precondition and is not checked on the device.
+ */
+#ifndef GDPA_H_
+#define GDPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdpa_status {
+  GDPA_OK = 0,
+  GDPA_ERR_INVALID = 1,
+  GDPA_ERR_UNSUPPORTED = 2,
+  GDPA_ERR_CUDA = 3,
+  GDPA_ERR_WORKSPACE = 4,
+  GDPA_ERR_TIMEOUT = 5
+} gdpa_status;
+
+/* Storage type of q, k, v. out/dout/dq/dk/dv use the same type, except that
+ * the FP8 forward writes bf16 out. */
+typedef enum gdpa_dtype { GDPA_BF16 = 0, GDPA_FP16 = 1, GDPA_E4M3 = 2 } gdpa_dtype;
+
+/* Activations ("Features" on the gdpa/README.md page). GELU_TANH is
+ * GELUApprox; FAST_GELU evaluates the same tanh-form GELU; LEAKY_RELU uses
+ * slope 0.01; derivatives at kinks follow PyTorch. */
+typedef enum gdpa_act {
+  GDPA_ACT_IDENTITY = 0,
+  GDPA_ACT_GELU = 1,
+  GDPA_ACT_GELU_TANH = 2,
+  GDPA_ACT_FAST_GELU = 3,
+  GDPA_ACT_RELU = 4,
+  GDPA_ACT_RELU2 = 5,
+  GDPA_ACT_LEAKY_RELU = 6,
+  GDPA_ACT_SILU = 7,
+  GDPA_ACT_HARDSWISH = 8,
+  GDPA_ACT_SOFTMAX = 9
+} gdpa_act;
+
+typedef struct gdpa_shape {
+  int batch;   /* number of sequences B (>= 0) */
+  int total_q; /* rows of q and out: sum of query lengths (B*max_seqlen_q when cu_seqlens_q is NULL) */
+  int total_k; /* rows of k and v */
+  int h_q;     /* query heads */
+  int h_kv;    /* key/value heads; h_q % h_kv == 0 (MHA, GQA, MQA) */
+  int d_qk;    /* head dim of q and k */
+  int d_v;     /* head dim of v and out */
+  int dtype;   /* gdpa_dtype */
+} gdpa_shape;
+
+/* Bytes of device workspace that gdpa_fwd (is_bwd = 0) or gdpa_bwd
+ * (is_bwd = 1) needs for this problem; 0 for an invalid shape. The size
+ * depends only on the arguments given here. */
+size_t gdpa_workspace_bytes(const gdpa_shape* shape, int max_seqlen_q, int max_seqlen_k, int is_bwd);
+
+/* Forward. scale multiplies Q K^T before the activation (1/sqrt(d_qk) is the
+ * usual choice). causal != 0 aligns query i of a length-Lq sequence with key
+ * i + Lk - Lq and allows keys at or before it. window > 0 limits each query
+ * to keys at distance < window from that position (with causal: the window
+ * keys ending at it); window <= 0 disables it. descale_qkv: FP8 only, device
+ * float[3] of per-tensor scales (q, k, v) so that value = code * scale; NULL
+ * otherwise. lse: required (device float [h_q, total_q]) for
+ * GDPA_ACT_SOFTMAX, ignored (may be NULL) otherwise. All device pointers
+ * must be 16-byte aligned. */
+int gdpa_fwd(const gdpa_shape* shape, const void* q, const void* k, const void* v,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+             int max_seqlen_k, int act, float scale, int causal, int window,
+             const float* descale_qkv, void* out, float* lse, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/* Backward (bf16/fp16 only). Arguments as for gdpa_fwd; out and lse are read
+ * only for GDPA_ACT_SOFTMAX (they must be the forward's results) and may be
+ * NULL otherwise. dout has out's layout; dq, dk, dv have q's, k's and v's.
+ * dq is accumulated in fp32 inside the workspace and converted at the end;
+ * dk/dv of a kv head sum the contributions of its query-head group.
+ * deterministic != 0 is reserved for an ordered dQ reduction; the current
+ * build accepts only 0 and returns GDPA_ERR_UNSUPPORTED otherwise. */
+int gdpa_bwd(const gdpa_shape* shape, const void* q, const void* k, const void* v,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+             int max_seqlen_k, int act, float scale, int causal, int window, const void* out,
+             const float* lse, const void* dout, void* dq, void* dk, void* dv, int deterministic,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device-side status of
+ * the current device (GDPA_OK or GDPA_ERR_TIMEOUT), or GDPA_ERR_CUDA if
+ * the synchronisation itself failed. */
+int gdpa_get_status(void* stream);
+
+/* Static, human-readable text for a status code. */
+const char* gdpa_error_string(int status);
+
+/* Number of multiprocessors the persistent kernels are sized for on the
+ * current device (the grid of every main kernel), or -1 on error. */
+int gdpa_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDPA_H_ */

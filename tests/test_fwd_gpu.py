@@ -1,0 +1,91 @@
+"""GPU forward parity: the CUDA path through the C-ABI against the float64 oracle,
+element by element, on seeded inputs that span several tiles and ragged tails."""
+
+import pytest
+import torch
+
+from generalized_attention_recsys_gb300 import inputs
+from gpu_util import FP8_TOL, FWD_TOL, assert_close, ref_fwd, run_fwd
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 127, 128, 129, 300, 0, 513, 64]
+ALL_ACTS = ["identity", "gelu", "gelu_tanh", "fast_gelu", "relu", "relu2", "leaky_relu", "silu",
+            "hardswish", "softmax"]
+
+
+def test_tiny_fixed_length():
+    inp = inputs.make_inputs(inputs.WORKLOADS["tiny_fixed"], seed=0)
+    out, _ = run_fwd(inp)
+    ref, _ = ref_fwd(inp)
+    assert_close(out, ref, FWD_TOL, "out")
+
+
+@pytest.mark.parametrize("act", ALL_ACTS)
+def test_every_activation_jagged(act):
+    inp = inputs.custom(len(RAGGED), 2, 2, 128, 128, RAGGED, RAGGED, act, seed=1)
+    out, lse = run_fwd(inp)
+    ref, ref_lse = ref_fwd(inp)
+    assert_close(out, ref, FWD_TOL, f"out[{act}]")
+    if act == "softmax":
+        fin = torch.isfinite(ref_lse)
+        assert torch.equal(torch.isfinite(lse.cpu()), fin)
+        assert (lse.cpu().double()[fin] - ref_lse[fin]).abs().max() < 1e-3
+
+
+@pytest.mark.parametrize("causal,window", [(True, -1), (True, 37), (False, 37), (True, 200), (False, 300)])
+@pytest.mark.parametrize("h_kv", [4, 2, 1])
+def test_masks_and_heads(causal, window, h_kv):
+    lq = [100, 257, 3, 0, 130, 129]
+    lk = [300, 257, 0, 5, 64, 400]
+    inp = inputs.custom(6, 4, h_kv, 128, 128, lq, lk, "silu", causal=causal, window=window, seed=2)
+    out, _ = run_fwd(inp)
+    ref, _ = ref_fwd(inp)
+    assert_close(out, ref, FWD_TOL, f"out causal={causal} window={window} h_kv={h_kv}")
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (96, 96), (192, 128)])
+@pytest.mark.parametrize("act", ["gelu", "softmax"])
+def test_head_dims(dims, act):
+    inp = inputs.custom(5, 4, 2, dims[0], dims[1], [130, 1, 256, 300, 77], [130, 1, 256, 300, 77], act,
+                        causal=True, seed=3)
+    out, _ = run_fwd(inp)
+    ref, _ = ref_fwd(inp)
+    assert_close(out, ref, FWD_TOL, f"out dims={dims}")
+
+
+@pytest.mark.parametrize("act", ["gelu_tanh", "softmax", "relu2"])
+def test_fp16(act):
+    inp = inputs.custom(4, 2, 2, 128, 128, [129, 256, 7, 400], [129, 256, 7, 400], act, dtype="fp16", seed=4)
+    out, _ = run_fwd(inp)
+    assert out.dtype == torch.float16
+    ref, _ = ref_fwd(inp)
+    assert_close(out, ref, FWD_TOL, "out fp16")
+
+
+@pytest.mark.parametrize("dims,h_kv,causal,window", [((128, 128), 4, False, -1), ((192, 128), 1, True, 100),
+                                                    ((64, 64), 2, True, -1)])
+def test_fp8(dims, h_kv, causal, window):
+    lens = [200, 129, 1, 450]
+    inp = inputs.custom(4, 4, h_kv, dims[0], dims[1], lens, lens, "fast_gelu", causal=causal, window=window,
+                        dtype="e4m3", seed=5, with_dout=False)
+    out, _ = run_fwd(inp)
+    assert out.dtype == torch.bfloat16
+    ref, _ = ref_fwd(inp)
+    assert_close(out, ref, FP8_TOL, "out e4m3")
+
+
+def test_zero_keys_give_zero_rows_and_empty_batch():
+    inp = inputs.custom(3, 2, 2, 64, 64, [50, 0, 130], [0, 10, 0], "gelu", seed=6)
+    out, _ = run_fwd(inp)
+    assert torch.count_nonzero(out) == 0
+    inp = inputs.custom(2, 2, 1, 64, 64, [0, 0], [0, 0], "gelu", seed=6)
+    out, _ = run_fwd(inp)
+    assert out.numel() == 0
+
+
+def test_repeat_calls_are_bitwise_stable():
+    inp = inputs.custom(len(RAGGED), 2, 2, 128, 128, RAGGED, RAGGED, "gelu", seed=7)
+    a, _ = run_fwd(inp)
+    b, _ = run_fwd(inp)
+    assert torch.equal(a, b)

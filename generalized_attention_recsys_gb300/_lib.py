@@ -22,7 +22,7 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 ACTS = {"identity": 0, "gelu": 1, "gelu_tanh": 2, "fast_gelu": 3, "relu": 4, "relu2": 5,
         "leaky_relu": 6, "silu": 7, "hardswish": 8, "softmax": 9}
 EXPORTS = ("gdpa_workspace_bytes", "gdpa_fwd", "gdpa_bwd", "gdpa_get_status", "gdpa_error_string",
-           "gdpa_num_sms")
+           "gdpa_set_profile_events", "gdpa_num_sms")
 
 
 class GdpaShape(ctypes.Structure):
@@ -65,6 +65,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdpa_get_status.restype = ci
         lib.gdpa_error_string.argtypes = [ci]
         lib.gdpa_error_string.restype = ctypes.c_char_p
+        lib.gdpa_set_profile_events.argtypes = [vp, vp]
+        lib.gdpa_set_profile_events.restype = ci
         lib.gdpa_num_sms.argtypes = []
         lib.gdpa_num_sms.restype = ci
         _lib = lib
@@ -171,3 +173,21 @@ def gdpa_get_status(stream=None) -> int:
 
 def gdpa_num_sms() -> int:
     return int(load().gdpa_num_sms())
+
+
+def gdpa_set_profile_events(before_main=None, after_main=None) -> None:
+    """Brackets the main kernel of later calls on this thread with two events.
+
+    Accepts torch.cuda.Event objects (they are recorded once here so that the
+    underlying CUDA events exist) or raw handles; None, None clears the hook.
+    """
+    def handle(ev):
+        if ev is None:
+            return None
+        if isinstance(ev, torch.cuda.Event):
+            if ev.cuda_event == 0:
+                ev.record()
+            return ev.cuda_event
+        return int(ev)
+
+    _check(load().gdpa_set_profile_events(handle(before_main), handle(after_main)))

@@ -178,6 +178,12 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
   }
 }
 
+thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
+
+void mark(cudaEvent_t ev, cudaStream_t stream) {
+  if (ev) cudaEventRecord(ev, stream);
+}
+
 Problem make_problem(const gdpa_shape* s, const int32_t* cu_q, const int32_t* cu_k, int max_q, int max_k,
                      int causal, int window) {
   Problem pb;
@@ -254,12 +260,14 @@ int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.work = wl;
   a.status = status;
   cudaError_t e;
+  mark(t_ev_before, stream);
   switch (s->d_qk) {
     case 64: e = launch_fwd_d64(s->dtype, tq, tk, tv, a, nsm, stream); break;
     case 96: e = launch_fwd_d96(s->dtype, tq, tk, tv, a, nsm, stream); break;
     case 128: e = launch_fwd_d128(s->dtype, tq, tk, tv, a, nsm, stream); break;
     default: e = launch_fwd_d192(s->dtype, tq, tk, tv, a, nsm, stream); break;
   }
+  mark(t_ev_after, stream);
   return e == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
@@ -270,6 +278,7 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   int st = validate(s, max_q, max_k, act, causal, window);
   if (st != GDPA_OK) return st;
   if (s->dtype == GDPA_E4M3) return GDPA_ERR_UNSUPPORTED;
+  if (s->d_qk > 128) return GDPA_ERR_UNSUPPORTED;  // (192,128) backward: TMEM plan holds dims <= 128
   if (deterministic) return GDPA_ERR_UNSUPPORTED;
   if (s->batch == 0 || (s->total_q == 0 && s->total_k == 0)) return GDPA_OK;
   if ((cu_q == nullptr) != (cu_k == nullptr)) return GDPA_ERR_INVALID;
@@ -323,7 +332,7 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
       !make_map(&tv, v, s->total_k, s->h_kv, s->d_v, s->dtype, workspace) ||
       !make_map(&tdo, dout, s->total_q, s->h_q, s->d_v, s->dtype, workspace))
     return GDPA_ERR_CUDA;
-  const cudaError_t e = launch_bwd(tq, tk, tv, tdo, a, nsm, stream);
+  const cudaError_t e = launch_bwd(tq, tk, tv, tdo, a, nsm, stream, t_ev_before, t_ev_after);
   return e == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
@@ -353,5 +362,11 @@ const char* gdpa_error_string(int s) {
 }
 
 int gdpa_num_sms(void) { return sm_count(); }
+
+int gdpa_set_profile_events(void* before_main, void* after_main) {
+  t_ev_before = static_cast<cudaEvent_t>(before_main);
+  t_ev_after = static_cast<cudaEvent_t>(after_main);
+  return GDPA_OK;
+}
 
 }  // extern "C"

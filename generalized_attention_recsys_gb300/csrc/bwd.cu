@@ -1,11 +1,108 @@
-// Backward launcher (kernels added separately).
+// Backward launcher: clears the fp32 dQ accumulator (and, for softmax,
+// computes rowsum(dO * O)), runs the main kernel, then converts dQ.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "args.h"
 
 namespace gdpa {
 
-cudaError_t launch_bwd(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                       const BwdArgs&, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t launch_bwd_d64(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_d96(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_d128(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+
+namespace {
+
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+
+// Zero the dQ accumulator; softmax: drow[h, t] = sum_d dO[t, h, d] * O[t, h, d].
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_prep(float4* acc, size_t n4, const T* out, const T* dout, float* drow,
+                                                int total_q, int h_q, int d_v) {
+  const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = tid; i < n4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (drow == nullptr) return;
+  const size_t warp = tid / 32, nwarps = nthr / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t rows = static_cast<size_t>(total_q) * h_q;
+  for (size_t r = warp; r < rows; r += nwarps) {
+    const T* o = out + r * d_v;
+    const T* g = dout + r * d_v;
+    float sum = 0.f;
+    for (int d = lane; d < d_v; d += 32) sum += to_f(o[d]) * to_f(g[d]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) {
+      const size_t t = r / h_q, h = r - t * h_q;
+      drow[h * total_q + t] = sum;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+template <>
+__device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
+  __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T* dq) {
+  const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = tid; i < n4; i += nthr) store4<T>(dq + 4 * i, acc[i]);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdArgs& a, int grid, cudaStream_t stream, cudaEvent_t before, cudaEvent_t after) {
+  const size_t n4 = static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4;
+  const int eg = grid * 8;  // elementwise kernels: 8 blocks of 256 per SM
+  float* drow = a.act == 9 ? a.drow : nullptr;
+  if (a.dtype == DT_FP16)
+    bwd_prep<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<float4*>(a.dq_acc), n4,
+                                             static_cast<const __half*>(a.out), static_cast<const __half*>(a.dout),
+                                             drow, a.pb.total_q, a.pb.h_q, a.d_v);
+  else
+    bwd_prep<__nv_bfloat16><<<eg, 256, 0, stream>>>(
+        reinterpret_cast<float4*>(a.dq_acc), n4, static_cast<const __nv_bfloat16*>(a.out),
+        static_cast<const __nv_bfloat16*>(a.dout), drow, a.pb.total_q, a.pb.h_q, a.d_v);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (before) cudaEventRecord(before, stream);
+  switch (a.d_qk) {
+    case 64: e = launch_bwd_d64(a.dtype, tq, tk, tv, tdo, a, grid, stream); break;
+    case 96: e = launch_bwd_d96(a.dtype, tq, tk, tv, tdo, a, grid, stream); break;
+    case 128: e = launch_bwd_d128(a.dtype, tq, tk, tv, tdo, a, grid, stream); break;
+    default: return cudaErrorNotSupported;
+  }
+  if (e != cudaSuccess) return e;
+  if (after) cudaEventRecord(after, stream);
+  if (a.dtype == DT_FP16)
+    bwd_post<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4,
+                                             static_cast<__half*>(a.dq));
+  else
+    bwd_post<__nv_bfloat16><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4,
+                                                    static_cast<__nv_bfloat16*>(a.dq));
+  return cudaGetLastError();
 }
 
 }  // namespace gdpa

@@ -1,0 +1,530 @@
+// GDPA backward on sm_103a.
+//
+// For every sequence b, query head h and its kv head g (gdpa/README.md,
+// "Features": forward and backward kernels; the gradients of
+// O = where(M, act(scale * Q K^T), 0) V):
+//   dV_g += P^T dO,  dP = dO V^T,  dS = scale * where(M, dP * act'(Z), 0),
+//   dQ_h = dS K_g,   dK_g += dS^T Q_h.
+// Softmax mode (Dao-AILab/flash-attention overview): P = exp(Z - lse),
+// dS = scale * P * (dP - rowsum(dO * O)).
+//
+// A work item is one 128-row key block of one kv head. Its K and V tiles stay
+// in shared memory while the CTA walks every query head of the kv head's
+// group and every 128-row query block that sees the key block, so dK and dV
+// accumulate in TMEM without atomics (GQA/MQA heads summed in place). dQ is
+// reduced across key blocks with fp32 vector atomics into a workspace and
+// converted at the end.
+//
+// All products are computed transposed so that TMEM lanes are key rows:
+//   S^T  = K Q^T      (A = K   smem K-major,  B = Q   smem K-major)
+//   dP^T = V dO^T     (A = V   smem K-major,  B = dO  smem K-major)
+//   dV  += P^T dO     (A = P^T TMEM,          B = dO  smem MN-major)
+//   dK  += dS^T Q     (A = dS^T smem K-major, B = Q   smem MN-major)
+//   dQ   = dS K       (A = dS^T smem read MN-major, B = K smem MN-major)
+// TMEM (512 columns): S^T [0,128) with P^T written over it, dP^T [128,256)
+// reused for dQ once dP^T has been read, dV [256,256+dv), dK [384,384+dqk).
+//
+// Warp roles (512 threads): warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 the
+// activation groups (query columns 0-63 and 64-127 of each tile), warps
+// 12-15 drain dQ from TMEM into the fp32 accumulator.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "act.cuh"
+#include "args.h"
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace gdpa {
+
+template <int DQK_, int DV_, int DT_>
+struct BwdCfg {
+  static constexpr int DQK = DQK_, DV = DV_, DT = DT_;
+  static_assert(DT == DT_BF16 || DT == DT_FP16, "backward takes 16-bit inputs");
+  static_assert(DQK <= 128 && DV <= 128, "backward TMEM plan holds head dims up to 128");
+  static constexpr int BOX_ELEMS = 64;
+  static constexpr int BOX_BYTES = 128 * 128;
+  static constexpr int QK_BOXES = (DQK + 63) / 64;
+  static constexpr int V_BOXES = (DV + 63) / 64;
+  static constexpr int K_BYTES = QK_BOXES * BOX_BYTES;
+  static constexpr int V_BYTES = V_BOXES * BOX_BYTES;
+  static constexpr int Q_BYTES = K_BYTES;
+  static constexpr int DO_BYTES = V_BYTES;
+  static constexpr int DS_BYTES = 2 * BOX_BYTES;
+  static constexpr int STAGES = 2;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES =
+      1024 + K_BYTES + V_BYTES + STAGES * (Q_BYTES + DO_BYTES) + DS_BYTES + BAR_BYTES;
+  static_assert(SMEM_BYTES <= 232448, "tiles do not fit in shared memory");
+  static constexpr int K_STEP = 16;
+  static constexpr int S_MMAS = DQK / K_STEP;
+  static constexpr int DP_MMAS = DV / K_STEP;
+  static constexpr int T_MMAS = kTileQ / K_STEP;  // GEMMs whose K is a 128-row tile
+  static constexpr uint32_t FMT = DT == DT_BF16 ? 1u : 0u;
+  static constexpr uint32_t IDESC_S = idesc_make(128, 128, FMT, FMT, 0, 0);
+  static constexpr uint32_t IDESC_DV = idesc_make(128, DV, FMT, FMT, 0, 1);
+  static constexpr uint32_t IDESC_DK = idesc_make(128, DQK, FMT, FMT, 0, 1);
+  static constexpr uint32_t IDESC_DQ = idesc_make(128, DQK, FMT, FMT, 1, 1);
+  static constexpr int THREADS = 512;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128, T_DV = 256, T_DK = 384;
+};
+
+struct BwdItem {
+  int b, g, k0, q_start, lq, k_start, lk, krows;
+  int qlo, nq, nsteps;
+};
+
+__device__ __forceinline__ BwdItem bwd_decode(const BwdArgs& a, int pos) {
+  BwdItem it;
+  const Problem& pb = a.pb;
+  const int e = pos / pb.h_kv;
+  it.g = pos - e * pb.h_kv;
+  const int2 bb = a.work->items[e];
+  it.b = bb.x;
+  seq_bounds(pb.cu_q, it.b, pb.max_q, it.q_start, it.lq);
+  seq_bounds(pb.cu_k, it.b, pb.max_k, it.k_start, it.lk);
+  it.k0 = bb.y * kTileK;
+  int kr = it.lk - it.k0;
+  it.krows = kr < 0 ? 0 : (kr > kTileK ? kTileK : kr);
+  int rmin, rmax;
+  if (it.krows > 0 && query_range(it.k0, it.k0 + it.krows - 1, it.lq, it.lk, pb.causal, pb.window, rmin, rmax)) {
+    it.qlo = rmin / kTileQ;
+    it.nq = rmax / kTileQ - it.qlo + 1;
+  } else {
+    it.qlo = 0;
+    it.nq = 0;
+  }
+  it.nsteps = it.nq * pb.group;
+  return it;
+}
+
+// Query head and first row of step s of an item.
+__device__ __forceinline__ void bwd_step(const BwdItem& it, const Problem& pb, int s, int& h, int& q0) {
+  const int hh = s / it.nq;
+  h = it.g * pb.group + hh;
+  q0 = (it.qlo + (s - hh * it.nq)) * kTileQ;
+}
+
+struct BwdSmem {
+  uint64_t kv_full, kv_empty;
+  uint64_t qd_full[2], qd_empty[2];
+  uint64_t s_full, ds_full, dq_full, dq_empty, acc_full, acc_empty;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  return DT == DT_BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// One 16-column chunk of the elementwise step: P^T to TMEM (over S^T) and
+// dS^T to the swizzled smem tile. Thread = key row `row`; columns are query
+// rows q0 + col0 .. col0 + 15 of the tile (col0 = 64*w + 16*c).
+template <class C, int ACT, bool MASKED>
+__device__ __forceinline__ void bwd_chunk(uint32_t t_lane, uint8_t* sDS, int row, int w, int c, float scale,
+                                          int c_lo, int c_hi, const float* lse_col, const float* d_col) {
+  const int col0 = 64 * w + 16 * c;
+  uint32_t r[32];
+  tmem_ld16(t_lane + C::T_S + col0, reinterpret_cast<uint32_t(&)[16]>(r[0]));
+  tmem_ld16(t_lane + C::T_DP + col0, reinterpret_cast<uint32_t(&)[16]>(r[16]));
+  tmem_ld_wait(r);
+  float p[16], ds[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float sv = __uint_as_float(r[e]);
+    const float dp = __uint_as_float(r[16 + e]);
+    float f, gr;
+    if constexpr (ACT == ACT_SOFTMAX) {
+      f = ex2_approx(sv * (scale * kLog2e) - lse_col[e] * kLog2e);
+      gr = (dp - d_col[e]) * f;  // dZ of softmax
+      gr *= scale;
+    } else {
+      act_value_grad<ACT>(sv * scale, f, gr);
+      gr *= scale * dp;
+    }
+    if (MASKED) {
+      const bool ok = (col0 + e) >= c_lo && (col0 + e) <= c_hi;
+      f = ok ? f : 0.0f;
+      gr = ok ? gr : 0.0f;
+    }
+    p[e] = f;
+    ds[e] = gr;
+  }
+  uint32_t pk[8], dk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    pk[i] = pack16<C::DT>(p[2 * i], p[2 * i + 1]);
+    dk[i] = pack16<C::DT>(ds[2 * i], ds[2 * i + 1]);
+  }
+  tmem_st8(t_lane + C::T_S + 64 * w + 8 * c, pk);
+  // dS^T row `row`, local columns 16c..16c+15 of box w: 16-byte chunks 2c and 2c+1, XOR-swizzled by row
+  uint8_t* base = sDS + w * C::BOX_BYTES + row * 128;
+  *reinterpret_cast<uint4*>(base + (((2 * c) ^ (row & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+  *reinterpret_cast<uint4*>(base + (((2 * c + 1) ^ (row & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+}
+
+template <class C, int ACT, bool MASKED>
+__device__ __forceinline__ void bwd_tile(uint32_t t_lane, uint8_t* sDS, int row, int w, float scale, int c_lo,
+                                         int c_hi, const float* lse, const float* drow, int col_base, int col_max) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float lc[16], dc[16];
+    if constexpr (ACT == ACT_SOFTMAX) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int idx = min(col_base + 64 * w + 16 * c + e, col_max);
+        lc[e] = __ldg(lse + idx);
+        dc[e] = __ldg(drow + idx);
+      }
+    }
+    bwd_chunk<C, ACT, MASKED>(t_lane, sDS, row, w, c, scale, c_lo, c_hi, lc, dc);
+  }
+}
+
+template <class C, bool MASKED>
+__device__ __forceinline__ void bwd_tile_dispatch(int act, uint32_t t_lane, uint8_t* sDS, int row, int w,
+                                                  float scale, int c_lo, int c_hi, const float* lse,
+                                                  const float* drow, int col_base, int col_max) {
+#define GDPA_BWD_CASE(A) \
+  case A: bwd_tile<C, A, MASKED>(t_lane, sDS, row, w, scale, c_lo, c_hi, lse, drow, col_base, col_max); break;
+  switch (act) {
+    GDPA_BWD_CASE(ACT_IDENTITY)
+    GDPA_BWD_CASE(ACT_GELU)
+    GDPA_BWD_CASE(ACT_GELU_TANH)
+    GDPA_BWD_CASE(ACT_FAST_GELU)
+    GDPA_BWD_CASE(ACT_RELU)
+    GDPA_BWD_CASE(ACT_RELU2)
+    GDPA_BWD_CASE(ACT_LEAKY_RELU)
+    GDPA_BWD_CASE(ACT_SILU)
+    GDPA_BWD_CASE(ACT_HARDSWISH)
+    default: bwd_tile<C, ACT_SOFTMAX, MASKED>(t_lane, sDS, row, w, scale, c_lo, c_hi, lse, drow, col_base, col_max);
+  }
+#undef GDPA_BWD_CASE
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    gdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::K_BYTES;
+  uint8_t* sQ = sV + C::V_BYTES;                    // STAGES x Q_BYTES
+  uint8_t* sDO = sQ + C::STAGES * C::Q_BYTES;       // STAGES x DO_BYTES
+  uint8_t* sDS = sDO + C::STAGES * C::DO_BYTES;     // 128 key rows x 128 query columns
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(sDS + C::DS_BYTES);
+  static_assert(sizeof(BwdSmem) <= C::BAR_BYTES, "barrier block too large");
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const Problem& pb = args.pb;
+  const int n_work = args.work->count * pb.h_kv;
+  const int G = gridDim.x;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.qd_full[i], 1);
+      mbar_init(&sm.qd_empty[i], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.ds_full, 256);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_empty, 128);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_empty, 256);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0, qd_it = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int pos = zigzag_pos(round, blockIdx.x, G);
+        if (pos >= n_work) break;
+        const BwdItem it = bwd_decode(args, pos);
+        if (it.nsteps == 0) continue;
+        ok = mbar_wait(&sm.kv_empty, (kv_cnt++ & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sm.kv_full, C::K_BYTES + C::V_BYTES);
+        for (int bx = 0; bx < C::QK_BOXES; ++bx)
+          tma_load_3d(sK + bx * C::BOX_BYTES, &tm_k, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
+        for (int bx = 0; bx < C::V_BOXES; ++bx)
+          tma_load_3d(sV + bx * C::BOX_BYTES, &tm_v, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
+        for (int s = 0; s < it.nsteps && ok; ++s) {
+          int h, q0;
+          bwd_step(it, pb, s, h, q0);
+          const int st = qd_it % 2;
+          ok = mbar_wait(&sm.qd_empty[st], ((qd_it / 2) & 1) ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&sm.qd_full[st], C::Q_BYTES + C::DO_BYTES);
+          for (int bx = 0; bx < C::QK_BOXES; ++bx)
+            tma_load_3d(sQ + st * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.qd_full[st], bx * 64, h,
+                        it.q_start + q0);
+          for (int bx = 0; bx < C::V_BOXES; ++bx)
+            tma_load_3d(sDO + st * C::DO_BYTES + bx * C::BOX_BYTES, &tm_do, &sm.qd_full[st], bx * 64, h,
+                        it.q_start + q0);
+          ++qd_it;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
+                     aDS = smem_u32(sDS);
+      auto issue_s = [&](int st) {
+        const uint32_t q = aQ + st * C::Q_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::S_MMAS; ++k) {
+          const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
+          mma_f16_ss(tbase + C::T_S, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), C::IDESC_S,
+                     k > 0);
+        }
+      };
+      auto issue_dp = [&](int st) {
+        const uint32_t d = aDO + st * C::DO_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::DP_MMAS; ++k) {
+          const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
+          mma_f16_ss(tbase + C::T_DP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(d + off, 16, 1024),
+                     C::IDESC_S, k > 0);
+        }
+      };
+      auto issue_grads = [&](int st, bool acc) {
+        const uint32_t q = aQ + st * C::Q_BYTES, d = aDO + st * C::DO_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::T_MMAS; ++k) {  // dV += P^T dO
+          const uint32_t a_t = tbase + C::T_S + 64 * (k / 4) + 8 * (k % 4);
+          mma_f16_ts(tbase + C::T_DV, a_t, sdesc_sw128(d + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DV,
+                     (acc || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < C::T_MMAS; ++k) {  // dK += dS^T Q
+          const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
+          mma_f16_ss(tbase + C::T_DK, sdesc_sw128(aDS + off, 16, 1024),
+                     sdesc_sw128(q + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DK, (acc || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < C::T_MMAS; ++k) {  // dQ = dS K
+          mma_f16_ss(tbase + C::T_DQ, sdesc_sw128(aDS + k * 2048, C::BOX_BYTES, 1024),
+                     sdesc_sw128(aK + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DQ, k > 0);
+        }
+      };
+      uint32_t kv_cnt = 0, qd_it = 0, ds_cnt = 0, dqe = 0, acce = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int pos = zigzag_pos(round, blockIdx.x, G);
+        if (pos >= n_work) break;
+        const BwdItem it = bwd_decode(args, pos);
+        if (it.nsteps == 0) continue;
+        ok = mbar_wait(&sm.kv_full, kv_cnt++ & 1, abort_flag);
+        if (ok) ok = mbar_wait(&sm.qd_full[qd_it % 2], (qd_it / 2) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(qd_it % 2);
+        ok = mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(qd_it % 2);
+        mma_commit(&sm.s_full);
+        for (int s = 0; s < it.nsteps; ++s) {
+          const int st = qd_it % 2;
+          ok = mbar_wait(&sm.ds_full, ds_cnt++ & 1, abort_flag);
+          if (ok && s == 0) ok = mbar_wait(&sm.acc_empty, (acce++ & 1) ^ 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_grads(st, s > 0);
+          mma_commit(&sm.dq_full);
+          mma_commit(&sm.qd_empty[st]);
+          ++qd_it;
+          if (s == it.nsteps - 1) {
+            mma_commit(&sm.acc_full);
+            mma_commit(&sm.kv_empty);
+          } else {
+            const int st2 = qd_it % 2;
+            ok = mbar_wait(&sm.qd_full[st2], (qd_it / 2) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(st2);
+            ok = mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(st2);
+            mma_commit(&sm.s_full);
+          }
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------ elementwise groups + dK/dV epilogue
+    const int w = (warp - 4) / 4;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // key row within the block
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    using T = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
+    const bool softmax = args.act == ACT_SOFTMAX;
+    uint32_t s_cnt = 0, acc_cnt = 0;
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+      const int pos = zigzag_pos(round, blockIdx.x, G);
+      if (pos >= n_work) break;
+      const BwdItem it = bwd_decode(args, pos);
+      const int kk = it.k0 + row;
+      const bool row_valid = row < it.krows;
+      // this group stores dV (w = 0) or dK (w = 1) of the block
+      const int ncols = w == 0 ? C::DV : C::DQK;
+      T* dst = reinterpret_cast<T*>(w == 0 ? args.dv : args.dk) +
+               (static_cast<size_t>(it.k_start + kk) * pb.h_kv + it.g) * ncols;
+      if (it.nsteps == 0) {
+        if (row_valid)
+          for (int q4 = 0; q4 < ncols * 2 / 16; ++q4) reinterpret_cast<uint4*>(dst)[q4] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      int qmin = 1, qmax = 0;
+      if (!(row_valid && query_range(kk, kk, it.lq, it.lk, pb.causal, pb.window, qmin, qmax))) {
+        qmin = 1;
+        qmax = 0;
+      }
+      for (int s = 0; s < it.nsteps; ++s) {
+        int h, q0;
+        bwd_step(it, pb, s, h, q0);
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full, s_cnt++ & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const int c_lo = qmin - q0, c_hi = qmax - q0;
+        const float* lse = softmax ? args.lse + static_cast<size_t>(h) * pb.total_q : nullptr;
+        const float* drow = softmax ? args.drow + static_cast<size_t>(h) * pb.total_q : nullptr;
+        const int col_base = it.q_start + q0;
+        const int col_max = pb.total_q - 1;
+        if (__all_sync(0xffffffffu, c_lo <= 64 * w && c_hi >= 64 * w + 63))
+          bwd_tile_dispatch<C, false>(args.act, t_lane, sDS, row, w, args.scale, c_lo, c_hi, lse, drow, col_base,
+                                      col_max);
+        else
+          bwd_tile_dispatch<C, true>(args.act, t_lane, sDS, row, w, args.scale, c_lo, c_hi, lse, drow, col_base,
+                                     col_max);
+        tmem_st_wait();
+        fence_async_shared();
+        tc_fence_before();
+        mbar_arrive(&sm.ds_full);
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, acc_cnt++ & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_acc = t_lane + (w == 0 ? C::T_DV : C::T_DK);
+#pragma unroll 1
+      for (int ch = 0; ch < ncols / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(t_acc + ch * 32, o);
+        tmem_ld_wait(o);
+        if (row_valid) {
+          uint32_t wv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) wv[e] = pack16<C::DT>(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) d4[q4] = make_uint4(wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.acc_empty);
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------ dQ drain: TMEM -> fp32 atomics
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // query row within the tile
+    const uint32_t t_dq = tbase + (static_cast<uint32_t>(quad * 32) << 16) + C::T_DQ;
+    uint32_t dq_cnt = 0;
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+      const int pos = zigzag_pos(round, blockIdx.x, G);
+      if (pos >= n_work) break;
+      const BwdItem it = bwd_decode(args, pos);
+      for (int s = 0; s < it.nsteps; ++s) {
+        int h, q0;
+        bwd_step(it, pb, s, h, q0);
+        const int qq = q0 + row;
+        const bool valid = qq < it.lq;
+        float* dst = args.dq_acc + (static_cast<size_t>(it.q_start + qq) * pb.h_q + h) * C::DQK;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_full, dq_cnt++ & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < C::DQK / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(t_dq + ch * 32, o);
+          tmem_ld_wait(o);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              red_add_v4(dst + ch * 32 + 4 * i, __uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                         __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+      }
+    }
+  }
+
+  // ------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort_flag) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+    if (threadIdx.x == 0) atomicExch(args.status, 5);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int DQK, int DV, int DT>
+cudaError_t launch_bwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+  using C = BwdCfg<DQK, DV, DT>;
+  auto kern = gdpa_bwd_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace gdpa

@@ -40,7 +40,7 @@
  * Errors. Problems visible on the host are returned before any launch:
  * GDPA_ERR_INVALID (null or misaligned pointer, negative size, h_q % h_kv,
  * bad enum), GDPA_ERR_UNSUPPORTED (head dims other than (64,64), (96,96),
- * (128,128), (192,128); FP8 backward), GDPA_ERR_WORKSPACE (too small),
+ * (128,128), (192,128); FP8 or (192,128) backward), GDPA_ERR_WORKSPACE (too small),
  * GDPA_ERR_CUDA (a launch or tensor-map encode failed). Every device-side wait
  * is bounded; a wait that gives up records GDPA_ERR_TIMEOUT in a per-device
  * status word that gdpa_get_status() returns. cu_seqlens consistency
@@ -137,6 +137,14 @@ int gdpa_get_status(void* stream);
 
 /* Static, human-readable text for a status code. */
 const char* gdpa_error_string(int status);
+
+/* Timing hook. When set, every later gdpa_fwd / gdpa_bwd call made by this
+ * host thread records `before_main` (a cudaEvent_t passed as void*) on its
+ * stream right before the main GDPA kernel launch and `after_main` right
+ * after it, so the pair brackets that kernel alone (not the work-list,
+ * dQ-clear or dQ-convert kernels). Pass NULL, NULL to stop. The events are
+ * owned by the caller and must stay valid while set. Returns GDPA_OK. */
+int gdpa_set_profile_events(void* before_main, void* after_main);
 
 /* Number of multiprocessors the persistent kernels are sized for on the
  * current device (the grid of every main kernel), or -1 on error. */

@@ -17,12 +17,14 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdpa.so")
 
-GDPA_OK, GDPA_ERR_INVALID, GDPA_ERR_UNSUPPORTED, GDPA_ERR_CUDA, GDPA_ERR_WORKSPACE, GDPA_ERR_TIMEOUT = range(6)
+(GDPA_OK, GDPA_ERR_INVALID, GDPA_ERR_UNSUPPORTED, GDPA_ERR_CUDA, GDPA_ERR_WORKSPACE, GDPA_ERR_TIMEOUT,
+ GDPA_ERR_SCRATCH_LIMIT) = range(7)
+NOALLOC_SCRATCH_BYTES = 512 * 1024
 DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 ACTS = {"identity": 0, "gelu": 1, "gelu_tanh": 2, "fast_gelu": 3, "relu": 4, "relu2": 5,
         "leaky_relu": 6, "silu": 7, "hardswish": 8, "softmax": 9}
 EXPORTS = ("gdpa_workspace_bytes", "gdpa_fwd", "gdpa_bwd", "gdpa_get_status", "gdpa_error_string",
-           "gdpa_set_profile_events", "gdpa_num_sms")
+           "gdpa_set_profile_events", "gdpa_fwd_noalloc", "gdpa_num_sms")
 
 
 class GdpaShape(ctypes.Structure):
@@ -67,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdpa_error_string.restype = ctypes.c_char_p
         lib.gdpa_set_profile_events.argtypes = [vp, vp]
         lib.gdpa_set_profile_events.restype = ci
+        lib.gdpa_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, ci, ci, ci, cf, ci, ci, vp, vp, vp, vp]
+        lib.gdpa_fwd_noalloc.restype = ci
         lib.gdpa_num_sms.argtypes = []
         lib.gdpa_num_sms.restype = ci
         _lib = lib
@@ -191,3 +195,28 @@ def gdpa_set_profile_events(before_main=None, after_main=None) -> None:
         return int(ev)
 
     _check(load().gdpa_set_profile_events(handle(before_main), handle(after_main)))
+
+
+def gdpa_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, act,
+                     scale: float, causal: bool = False, window: int = -1, descale_qkv=None, out=None, lse=None,
+                     batch=None, stream=None):
+    """C-ABI gdpa_fwd_noalloc: the forward with the library's fixed scratch
+    instead of a workspace (for callers that cannot allocate device memory;
+    the library itself allocates nothing). `out`/`lse` are allocated here only
+    when not given. Calls sharing a device must not overlap on the GPU."""
+    lib = load()
+    if batch is None:
+        batch = cu_seqlens_q.numel() - 1 if cu_seqlens_q is not None else q.shape[0] // max(max_seqlen_q, 1)
+    shape = make_shape(q, k, v, batch)
+    a = _act(act)
+    if out is None:
+        odt = torch.bfloat16 if q.dtype == torch.float8_e4m3fn else q.dtype
+        out = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=odt, device=q.device)
+    if a == ACTS["softmax"] and lse is None:
+        lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    st = lib.gdpa_fwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
+                              _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k), a, float(scale),
+                              int(bool(causal)), int(window), _ptr(descale_qkv), _ptr(out), _ptr(lse),
+                              _stream(stream))
+    _check(st)
+    return out, (lse if a == ACTS["softmax"] else None)

@@ -357,6 +357,7 @@ const char* gdpa_error_string(int s) {
     case GDPA_ERR_CUDA: return "CUDA error";
     case GDPA_ERR_WORKSPACE: return "workspace missing or too small";
     case GDPA_ERR_TIMEOUT: return "device-side wait timed out";
+    case GDPA_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of the no-allocation forward";
     default: return "unknown status";
   }
 }
@@ -370,3 +371,48 @@ int gdpa_set_profile_events(void* before_main, void* after_main) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- forward without allocation
+//
+// For callers that cannot allocate device memory (see gdpa_fwd_noalloc in
+// gdpa.h): the forward's only scratch, the work list, lives in this fixed
+// array instead of a caller workspace. Host code must not pass the symbol
+// itself to a kernel (on the host it names a stand-in, not device memory);
+// it passes the address cudaGetSymbolAddress returns for the current device.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_fwd_noalloc_scratch[GDPA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and cached; NULL on failure.
+void* noalloc_scratch_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" int gdpa_fwd_noalloc(const gdpa_shape* s, const void* q, const void* k, const void* v,
+                                const int32_t* cu_q, const int32_t* cu_k, int max_q, int max_k, int act,
+                                float scale, int causal, int window, const float* descale, void* out, float* lse,
+                                void* stream) {
+  const int st = validate(s, max_q, max_k, act, causal, window);
+  if (st != GDPA_OK) return st;
+  const size_t need = gdpa_workspace_bytes(s, max_q, max_k, 0);
+  if (need > GDPA_NOALLOC_SCRATCH_BYTES) return GDPA_ERR_SCRATCH_LIMIT;
+  if (s->total_q == 0 || s->batch == 0) return GDPA_OK;
+  void* scratch = noalloc_scratch_ptr();
+  if (!scratch) return GDPA_ERR_CUDA;
+  return gdpa_fwd(s, q, k, v, cu_q, cu_k, max_q, max_k, act, scale, causal, window, descale, out, lse, scratch,
+                  GDPA_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -63,7 +63,8 @@ typedef enum gdpa_status {
   GDPA_ERR_UNSUPPORTED = 2,
   GDPA_ERR_CUDA = 3,
   GDPA_ERR_WORKSPACE = 4,
-  GDPA_ERR_TIMEOUT = 5
+  GDPA_ERR_TIMEOUT = 5,
+  GDPA_ERR_SCRATCH_LIMIT = 6 /* problem too large for gdpa_fwd_noalloc's fixed scratch */
 } gdpa_status;
 
 /* Storage type of q, k, v. out/dout/dq/dk/dv use the same type, except that
@@ -145,6 +146,36 @@ const char* gdpa_error_string(int status);
  * dQ-clear or dQ-convert kernels). Pass NULL, NULL to stop. The events are
  * owned by the caller and must stay valid while set. Returns GDPA_OK. */
 int gdpa_set_profile_events(void* before_main, void* after_main);
+
+/* Forward without any allocation. No counterpart on the pages: this is an
+ * addition of this library for callers that cannot call cudaMalloc -- for
+ * example a plugin running inside a host framework whose device memory is
+ * owned entirely by that framework's allocator, or a deployment that forbids
+ * allocations after start-up to keep a fixed, pre-planned memory footprint.
+ *
+ * Same arguments and results as gdpa_fwd, minus the workspace: the scratch
+ * that gdpa_fwd takes from `workspace` (the cost-sorted work list) lives
+ * instead in a fixed device array of GDPA_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. The caller still allocates q, k, v, out, lse and the cu_seqlens.
+ *
+ * - Problems whose work list needs more than GDPA_NOALLOC_SCRATCH_BYTES
+ *   (gdpa_workspace_bytes(shape, ..., 0) above it) return
+ *   GDPA_ERR_SCRATCH_LIMIT before anything is launched.
+ * - The first call on each device looks up that device's address of the
+ *   array (cudaGetSymbolAddress, with the device current); make that first
+ *   call before any stream capture.
+ * - The call allocates nothing: no cudaMalloc, cudaFree or allocating
+ *   library routine.
+ * - All calls on a device share the one array and each call rewrites it
+ *   completely before reading it (nothing in it has to start at zero), so
+ *   calls that overlap on the GPU -- on different streams or from
+ *   different host threads -- race and must be serialised by the caller. */
+#define GDPA_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+int gdpa_fwd_noalloc(const gdpa_shape* shape, const void* q, const void* k, const void* v,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+                     int max_seqlen_k, int act, float scale, int causal, int window,
+                     const float* descale_qkv, void* out, float* lse, void* stream);
 
 /* Number of multiprocessors the persistent kernels are sized for on the
  * current device (the grid of every main kernel), or -1 on error. */

@@ -103,3 +103,13 @@ def test_null_and_misaligned_pointers_rejected(lib):
     s2 = _shape(total_q=250)
     assert lib.gdpa_fwd(ctypes.byref(s2), aligned, aligned, aligned, None, None, 128, 128, 1, 0.1, 0, -1,
                         None, aligned, None, aligned, 1 << 20, None) == _lib.GDPA_ERR_INVALID
+
+
+def test_noalloc_forward_rejects_problems_beyond_its_scratch(lib):
+    # the work list of 70,000 one-token sequences needs more than the fixed scratch
+    s = _shape(batch=70000, total_q=70000, total_k=70000)
+    assert _lib.gdpa_workspace_bytes(s, 1, 1, False) > _lib.NOALLOC_SCRATCH_BYTES
+    st = lib.gdpa_fwd_noalloc(ctypes.byref(s), None, None, None, None, None, 1, 1, 1, 0.1, 0, -1, None, None,
+                              None, None)
+    assert st == _lib.GDPA_ERR_SCRATCH_LIMIT
+    assert "scratch" in _lib.gdpa_error_string(st)

@@ -149,39 +149,49 @@ __device__ __forceinline__ void store_p_chunk(uint32_t taddr, const float (&p)[3
 
 // P = where(c_lo <= col <= c_hi, act(scale * S), 0) for one 128x128 tile;
 // thread = one row (TMEM lane), t_s = this lane's address of S column 0.
+// The load of the next 32 columns is in flight while the current ones are
+// activated; P chunk c goes to columns already read (P packs 2 or 4 values
+// per 32-bit column, so it never overtakes the S columns still to be read).
 template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ void act_tile(uint32_t t_s, float scale, int c_lo, int c_hi) {
-#pragma unroll 1
+__device__ __forceinline__ void act_tile(uint32_t t_s, const ActConsts& k, int c_lo, int c_hi) {
+  uint32_t sa[32], sb[32];
+  tmem_ld32(t_s, sa);
+  tmem_ld_wait(sa);
+#pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
-    uint32_t s[32];
-    tmem_ld32(t_s + ch * 32, s);
-    tmem_ld_wait(s);
+    uint32_t(&cur)[32] = (ch & 1) ? sb : sa;
+    uint32_t(&nxt)[32] = (ch & 1) ? sa : sb;
+    if (ch < 3) tmem_ld32(t_s + (ch + 1) * 32, nxt);
     float p[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      float v = act_value<ACT>(__uint_as_float(s[e]) * scale);
+    for (int e = 0; e < 16; ++e) {
+      const f2_t r = act_pair<ACT>(f2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), k);
+      float v0 = f2_lo(r), v1 = f2_hi(r);
       if (MASKED) {
-        const int c = ch * 32 + e;
-        v = (c >= c_lo && c <= c_hi) ? v : 0.0f;
+        const int c0 = ch * 32 + 2 * e;
+        v0 = (c0 >= c_lo && c0 <= c_hi) ? v0 : 0.0f;
+        v1 = (c0 + 1 >= c_lo && c0 + 1 <= c_hi) ? v1 : 0.0f;
       }
-      p[e] = v;
+      p[2 * e] = v0;
+      p[2 * e + 1] = v1;
     }
     store_p_chunk<C::DT>(t_s + ch * C::P_COLS_PER_CHUNK, p);
+    if (ch < 3) tmem_ld_wait(nxt);
   }
 }
 
 template <class C, bool MASKED>
-__device__ __forceinline__ void act_tile_dispatch(int act, uint32_t t_s, float scale, int c_lo, int c_hi) {
+__device__ __forceinline__ void act_tile_dispatch(int act, uint32_t t_s, const ActConsts& k, int c_lo, int c_hi) {
   switch (act) {
-    case ACT_IDENTITY: act_tile<C, ACT_IDENTITY, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_GELU: act_tile<C, ACT_GELU, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_GELU_TANH: act_tile<C, ACT_GELU_TANH, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_FAST_GELU: act_tile<C, ACT_FAST_GELU, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_RELU: act_tile<C, ACT_RELU, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_RELU2: act_tile<C, ACT_RELU2, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_LEAKY_RELU: act_tile<C, ACT_LEAKY_RELU, MASKED>(t_s, scale, c_lo, c_hi); break;
-    case ACT_SILU: act_tile<C, ACT_SILU, MASKED>(t_s, scale, c_lo, c_hi); break;
-    default: act_tile<C, ACT_HARDSWISH, MASKED>(t_s, scale, c_lo, c_hi); break;
+    case ACT_IDENTITY: act_tile<C, ACT_IDENTITY, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_GELU: act_tile<C, ACT_GELU, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_GELU_TANH: act_tile<C, ACT_GELU_TANH, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_FAST_GELU: act_tile<C, ACT_FAST_GELU, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_RELU: act_tile<C, ACT_RELU, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_RELU2: act_tile<C, ACT_RELU2, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_LEAKY_RELU: act_tile<C, ACT_LEAKY_RELU, MASKED>(t_s, k, c_lo, c_hi); break;
+    case ACT_SILU: act_tile<C, ACT_SILU, MASKED>(t_s, k, c_lo, c_hi); break;
+    default: act_tile<C, ACT_HARDSWISH, MASKED>(t_s, k, c_lo, c_hi); break;
   }
 }
 
@@ -442,6 +452,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       v_scale = args.descale[2];
     }
     const float s_scale = softmax ? qk_scale * kLog2e : qk_scale;
+    const ActConsts act_k = make_act_consts(qk_scale);
     uint32_t sc = 0, oc = 0;
     using OutT = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
     OutT* out = reinterpret_cast<OutT*>(args.out);
@@ -469,9 +480,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (softmax) {
             softmax_tile<C>(t_s, t_o, j > it.lo[half], s_scale, c_lo, c_hi, m, l);
           } else if (__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kTileK - 1)) {
-            act_tile_dispatch<C, false>(args.act, t_s, s_scale, c_lo, c_hi);
+            act_tile_dispatch<C, false>(args.act, t_s, act_k, c_lo, c_hi);
           } else {
-            act_tile_dispatch<C, true>(args.act, t_s, s_scale, c_lo, c_hi);
+            act_tile_dispatch<C, true>(args.act, t_s, act_k, c_lo, c_hi);
           }
           tmem_st_wait();
           tc_fence_before();

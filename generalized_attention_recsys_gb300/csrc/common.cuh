@@ -8,7 +8,7 @@ namespace gdpa {
 
 constexpr int kTileQ = 128;   // query rows per Q tile (TMEM lanes)
 constexpr int kTileK = 128;   // key rows per KV block
-constexpr int kFwdItemRows = 2 * kTileQ;  // a forward work item holds two Q tiles of one (sequence, head)
+constexpr int kFwdItemRows = kTileQ;  // a forward work item is one Q tile of one (sequence, head)
 
 enum DType : int { DT_BF16 = 0, DT_FP16 = 1, DT_E4M3 = 2 };
 

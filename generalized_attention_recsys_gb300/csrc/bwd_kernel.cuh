@@ -131,7 +131,7 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
 // dS^T to the swizzled smem tile. Thread = key row `row`; columns are query
 // rows q0 + col0 .. col0 + 15 of the tile (col0 = 64*w + 16*c).
 template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ void bwd_chunk(uint32_t t_lane, uint8_t* sDS, int row, int w, int c, float scale,
+__device__ __forceinline__ void bwd_chunk(uint32_t t_lane, uint8_t* sDS, int row, int w, int c, const BwdConsts& k,
                                           int c_lo, int c_hi, const float* lse_col, const float* d_col) {
   const int col0 = 64 * w + 16 * c;
   uint32_t r[32];
@@ -140,25 +140,31 @@ __device__ __forceinline__ void bwd_chunk(uint32_t t_lane, uint8_t* sDS, int row
   tmem_ld_wait(r);
   float p[16], ds[16];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const float sv = __uint_as_float(r[e]);
-    const float dp = __uint_as_float(r[16 + e]);
-    float f, gr;
+  for (int e = 0; e < 16; e += 2) {
+    const f2_t sv = f2(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+    const f2_t dp = f2(__uint_as_float(r[16 + e]), __uint_as_float(r[17 + e]));
+    f2_t f, gr;
     if constexpr (ACT == ACT_SOFTMAX) {
-      f = ex2_approx(sv * (scale * kLog2e) - lse_col[e] * kLog2e);
-      gr = (dp - d_col[e]) * f;  // dZ of softmax
-      gr *= scale;
+      // P = 2^(s scale log2e - lse log2e); dS = scale P (dP - rowsum(dO O))
+      const f2_t a = fma2(sv, f2(k.scale * kLog2e), f2(-lse_col[e] * kLog2e, -lse_col[e + 1] * kLog2e));
+      f = f2(ex2_approx(f2_lo(a)), ex2_approx(f2_hi(a)));
+      gr = mul2(mul2(add2(dp, f2(-d_col[e], -d_col[e + 1])), f), f2(k.scale));
     } else {
-      act_value_grad<ACT>(sv * scale, f, gr);
-      gr *= scale * dp;
+      act_pair_grad<ACT>(sv, dp, k, f, gr);
     }
+    float f0 = f2_lo(f), f1 = f2_hi(f), g0 = f2_lo(gr), g1 = f2_hi(gr);
     if (MASKED) {
-      const bool ok = (col0 + e) >= c_lo && (col0 + e) <= c_hi;
-      f = ok ? f : 0.0f;
-      gr = ok ? gr : 0.0f;
+      const bool ok0 = (col0 + e) >= c_lo && (col0 + e) <= c_hi;
+      const bool ok1 = (col0 + e + 1) >= c_lo && (col0 + e + 1) <= c_hi;
+      f0 = ok0 ? f0 : 0.0f;
+      g0 = ok0 ? g0 : 0.0f;
+      f1 = ok1 ? f1 : 0.0f;
+      g1 = ok1 ? g1 : 0.0f;
     }
-    p[e] = f;
-    ds[e] = gr;
+    p[e] = f0;
+    p[e + 1] = f1;
+    ds[e] = g0;
+    ds[e + 1] = g1;
   }
   uint32_t pk[8], dk[8];
 #pragma unroll
@@ -174,7 +180,7 @@ __device__ __forceinline__ void bwd_chunk(uint32_t t_lane, uint8_t* sDS, int row
 }
 
 template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ void bwd_tile(uint32_t t_lane, uint8_t* sDS, int row, int w, float scale, int c_lo,
+__device__ __forceinline__ void bwd_tile(uint32_t t_lane, uint8_t* sDS, int row, int w, const BwdConsts& k, int c_lo,
                                          int c_hi, const float* lse, const float* drow, int col_base, int col_max) {
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
@@ -187,16 +193,16 @@ __device__ __forceinline__ void bwd_tile(uint32_t t_lane, uint8_t* sDS, int row,
         dc[e] = __ldg(drow + idx);
       }
     }
-    bwd_chunk<C, ACT, MASKED>(t_lane, sDS, row, w, c, scale, c_lo, c_hi, lc, dc);
+    bwd_chunk<C, ACT, MASKED>(t_lane, sDS, row, w, c, k, c_lo, c_hi, lc, dc);
   }
 }
 
 template <class C, bool MASKED>
 __device__ __forceinline__ void bwd_tile_dispatch(int act, uint32_t t_lane, uint8_t* sDS, int row, int w,
-                                                  float scale, int c_lo, int c_hi, const float* lse,
+                                                  const BwdConsts& k, int c_lo, int c_hi, const float* lse,
                                                   const float* drow, int col_base, int col_max) {
 #define GDPA_BWD_CASE(A) \
-  case A: bwd_tile<C, A, MASKED>(t_lane, sDS, row, w, scale, c_lo, c_hi, lse, drow, col_base, col_max); break;
+  case A: bwd_tile<C, A, MASKED>(t_lane, sDS, row, w, k, c_lo, c_hi, lse, drow, col_base, col_max); break;
   switch (act) {
     GDPA_BWD_CASE(ACT_IDENTITY)
     GDPA_BWD_CASE(ACT_GELU)
@@ -207,7 +213,7 @@ __device__ __forceinline__ void bwd_tile_dispatch(int act, uint32_t t_lane, uint
     GDPA_BWD_CASE(ACT_LEAKY_RELU)
     GDPA_BWD_CASE(ACT_SILU)
     GDPA_BWD_CASE(ACT_HARDSWISH)
-    default: bwd_tile<C, ACT_SOFTMAX, MASKED>(t_lane, sDS, row, w, scale, c_lo, c_hi, lse, drow, col_base, col_max);
+    default: bwd_tile<C, ACT_SOFTMAX, MASKED>(t_lane, sDS, row, w, k, c_lo, c_hi, lse, drow, col_base, col_max);
   }
 #undef GDPA_BWD_CASE
 }
@@ -395,6 +401,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     using T = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
     const bool softmax = args.act == ACT_SOFTMAX;
+    const BwdConsts bwd_k = make_bwd_consts(args.scale);
     uint32_t s_cnt = 0, acc_cnt = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -429,10 +436,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int col_base = it.q_start + q0;
         const int col_max = pb.total_q - 1;
         if (__all_sync(0xffffffffu, c_lo <= 64 * w && c_hi >= 64 * w + 63))
-          bwd_tile_dispatch<C, false>(args.act, t_lane, sDS, row, w, args.scale, c_lo, c_hi, lse, drow, col_base,
+          bwd_tile_dispatch<C, false>(args.act, t_lane, sDS, row, w, bwd_k, c_lo, c_hi, lse, drow, col_base,
                                       col_max);
         else
-          bwd_tile_dispatch<C, true>(args.act, t_lane, sDS, row, w, args.scale, c_lo, c_hi, lse, drow, col_base,
+          bwd_tile_dispatch<C, true>(args.act, t_lane, sDS, row, w, bwd_k, c_lo, c_hi, lse, drow, col_base,
                                      col_max);
         tmem_st_wait();
         fence_async_shared();

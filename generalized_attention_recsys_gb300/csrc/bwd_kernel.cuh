@@ -24,9 +24,9 @@
 // TMEM (512 columns): S^T [0,128) with P^T written over it, dP^T [128,256)
 // reused for dQ once dP^T has been read, dV [256,256+dv), dK [384,384+dqk).
 //
-// Warp roles (512 threads): warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 the
-// activation groups (query columns 0-63 and 64-127 of each tile), warps
-// 12-15 drain dQ from TMEM into the fp32 accumulator.
+// Warp roles (128 * (NG + 2) threads): warp 0 TMA, warp 1 MMA, NG elementwise
+// groups of four warps (128 / NG query columns of each tile each), then four
+// warps that drain dQ from TMEM into the fp32 accumulator.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -69,8 +69,13 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DV = idesc_make(128, DV, FMT, FMT, 0, 1);
   static constexpr uint32_t IDESC_DK = idesc_make(128, DQK, FMT, FMT, 0, 1);
   static constexpr uint32_t IDESC_DQ = idesc_make(128, DQK, FMT, FMT, 1, 1);
-  static constexpr int THREADS = 512;
+  static constexpr int NG = 2;             // elementwise groups (4 warps each), 64 query columns each
+  static constexpr int GCOLS = kTileQ / NG;  // query columns per group
+  static constexpr int GCHUNKS = GCOLS / 16;
+  static constexpr int THREADS = 128 * (NG + 2);
+  static constexpr int ACT_WARP0 = 4, DRAIN_WARP0 = 4 + 4 * NG;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128, T_DV = 256, T_DK = 384;
+
 };
 
 struct BwdItem {
@@ -112,7 +117,7 @@ __device__ __forceinline__ void bwd_step(const BwdItem& it, const Problem& pb, i
 struct BwdSmem {
   uint64_t kv_full, kv_empty;
   uint64_t qd_full[2], qd_empty[2];
-  uint64_t s_full, ds_full, dq_full, dq_empty, acc_full, acc_empty;
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_full, acc_empty;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -127,82 +132,110 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return DT == DT_BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-// One 16-column chunk of the elementwise step: P^T to TMEM (over S^T) and
-// dS^T to the swizzled smem tile. Thread = key row `row`; columns are query
-// rows q0 + col0 .. col0 + 15 of the tile (col0 = 64*w + 16*c).
-template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ void bwd_chunk(uint32_t t_lane, uint8_t* sDS, int row, int w, int c, const BwdConsts& k,
-                                          int c_lo, int c_hi, const float* lse_col, const float* d_col) {
-  const int col0 = 64 * w + 16 * c;
-  uint32_t r[32];
-  tmem_ld16(t_lane + C::T_S + col0, reinterpret_cast<uint32_t(&)[16]>(r[0]));
-  tmem_ld16(t_lane + C::T_DP + col0, reinterpret_cast<uint32_t(&)[16]>(r[16]));
-  tmem_ld_wait(r);
-  float p[16], ds[16];
-#pragma unroll
-  for (int e = 0; e < 16; e += 2) {
-    const f2_t sv = f2(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-    const f2_t dp = f2(__uint_as_float(r[16 + e]), __uint_as_float(r[17 + e]));
-    f2_t f, gr;
-    if constexpr (ACT == ACT_SOFTMAX) {
-      // P = 2^(s scale log2e - lse log2e); dS = scale P (dP - rowsum(dO O))
-      const f2_t a = fma2(sv, f2(k.scale * kLog2e), f2(-lse_col[e] * kLog2e, -lse_col[e + 1] * kLog2e));
-      f = f2(ex2_approx(f2_lo(a)), ex2_approx(f2_hi(a)));
-      gr = mul2(mul2(add2(dp, f2(-d_col[e], -d_col[e + 1])), f), f2(k.scale));
-    } else {
-      act_pair_grad<ACT>(sv, dp, k, f, gr);
-    }
-    float f0 = f2_lo(f), f1 = f2_hi(f), g0 = f2_lo(gr), g1 = f2_hi(gr);
-    if (MASKED) {
-      const bool ok0 = (col0 + e) >= c_lo && (col0 + e) <= c_hi;
-      const bool ok1 = (col0 + e + 1) >= c_lo && (col0 + e + 1) <= c_hi;
-      f0 = ok0 ? f0 : 0.0f;
-      g0 = ok0 ? g0 : 0.0f;
-      f1 = ok1 ? f1 : 0.0f;
-      g1 = ok1 ? g1 : 0.0f;
-    }
-    p[e] = f0;
-    p[e + 1] = f1;
-    ds[e] = g0;
-    ds[e + 1] = g1;
-  }
-  uint32_t pk[8], dk[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    pk[i] = pack16<C::DT>(p[2 * i], p[2 * i + 1]);
-    dk[i] = pack16<C::DT>(ds[2 * i], ds[2 * i + 1]);
-  }
-  tmem_st8(t_lane + C::T_S + 64 * w + 8 * c, pk);
-  // dS^T row `row`, local columns 16c..16c+15 of box w: 16-byte chunks 2c and 2c+1, XOR-swizzled by row
-  uint8_t* base = sDS + w * C::BOX_BYTES + row * 128;
-  *reinterpret_cast<uint4*>(base + (((2 * c) ^ (row & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-  *reinterpret_cast<uint4*>(base + (((2 * c + 1) ^ (row & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+// The elementwise step runs in two passes per tile so that the tensor core
+// keeps working meanwhile (thread = key row `row`, group w owns query columns
+// [64 w, 64 w + 64)):
+//   pass 1 (needs S^T only; dP^T is still being computed): P^T = act(Z^T)
+//     and G^T = scale * act'(Z^T) (softmax: G^T = P^T), masked entries 0,
+//     both packed to 16 bits and written over the S^T columns just read:
+//     for query columns [64w + 32c, +32), P^T at TMEM column 64w + 32c and
+//     G^T at 64w + 32c + 16.
+//   pass 2 (needs dP^T; dV = P^T dO already runs): dS^T = dP^T * G^T
+//     (softmax: scale * G^T (dP^T - rowsum(dO O))) into the swizzled smem tile.
+template <class C>
+__host__ __device__ constexpr uint32_t pt_col(int k) {  // P^T columns of MMA k-step k (query cols 16k..16k+15)
+  return 64 * (k / 4) + 32 * ((k % 4) / 2) + 8 * (k % 2);
 }
 
 template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ void bwd_tile(uint32_t t_lane, uint8_t* sDS, int row, int w, const BwdConsts& k, int c_lo,
-                                         int c_hi, const float* lse, const float* drow, int col_base, int col_max) {
+__device__ __forceinline__ void bwd_pass1(uint32_t t_lane, int w, const BwdConsts& k, int c_lo, int c_hi,
+                                          const float* lse, int col_base, int col_max) {
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    float lc[16], dc[16];
-    if constexpr (ACT == ACT_SOFTMAX) {
+  for (int c = 0; c < 2; ++c) {
+    // chunk c's outputs land only in chunk c's own 32 S^T columns
+    const int col0 = 64 * w + 32 * c;
+    uint32_t cur[32];
+    tmem_ld32(t_lane + C::T_S + col0, cur);
+    tmem_ld_wait(cur);
+    uint32_t pk[16], gk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int idx = min(col_base + 64 * w + 16 * c + e, col_max);
-        lc[e] = __ldg(lse + idx);
-        dc[e] = __ldg(drow + idx);
+    for (int e = 0; e < 32; e += 2) {
+      const f2_t sv = f2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1]));
+      f2_t pv, gv;
+      if constexpr (ACT == ACT_SOFTMAX) {
+        const int i0 = min(col_base + col0 + e, col_max), i1 = min(col_base + col0 + e + 1, col_max);
+        const f2_t a = fma2(sv, f2(k.scale * kLog2e), f2(-__ldg(lse + i0) * kLog2e, -__ldg(lse + i1) * kLog2e));
+        pv = f2(ex2_approx(f2_lo(a)), ex2_approx(f2_hi(a)));
+        gv = pv;
+      } else {
+        act_pair_grad<ACT>(sv, f2(1.0f), k, pv, gv);
       }
+      float p0 = f2_lo(pv), p1 = f2_hi(pv), g0 = f2_lo(gv), g1 = f2_hi(gv);
+      if (MASKED) {
+        const bool ok0 = (col0 + e) >= c_lo && (col0 + e) <= c_hi;
+        const bool ok1 = (col0 + e + 1) >= c_lo && (col0 + e + 1) <= c_hi;
+        p0 = ok0 ? p0 : 0.0f;
+        g0 = ok0 ? g0 : 0.0f;
+        p1 = ok1 ? p1 : 0.0f;
+        g1 = ok1 ? g1 : 0.0f;
+      }
+      pk[e / 2] = pack16<C::DT>(p0, p1);
+      gk[e / 2] = pack16<C::DT>(g0, g1);
     }
-    bwd_chunk<C, ACT, MASKED>(t_lane, sDS, row, w, c, k, c_lo, c_hi, lc, dc);
+    tmem_st16(t_lane + C::T_S + col0, pk);
+    tmem_st16(t_lane + C::T_S + col0 + 16, gk);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float unpack_lo(uint32_t v) {
+  if constexpr (DT == DT_BF16) return __uint_as_float(v << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+template <int DT>
+__device__ __forceinline__ float unpack_hi(uint32_t v) {
+  if constexpr (DT == DT_BF16) return __uint_as_float(v & 0xFFFF0000u);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+}
+
+template <class C, bool SOFTMAX>
+__device__ __forceinline__ void bwd_pass2(uint32_t t_lane, uint8_t* sDS, int row, int w, float scale,
+                                          const float* drow, int col_base, int col_max) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int col0 = 64 * w + 32 * c;
+    uint32_t dp[32], g[16];
+    tmem_ld32(t_lane + C::T_DP + col0, dp);
+    tmem_ld16(t_lane + C::T_S + col0 + 16, g);
+    tmem_ld_wait(dp);
+    tmem_ld_wait(g);
+    uint32_t dk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      f2_t gv = f2(unpack_lo<C::DT>(g[e]), unpack_hi<C::DT>(g[e]));
+      f2_t dv = f2(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1]));
+      if constexpr (SOFTMAX) {
+        const int i0 = min(col_base + col0 + 2 * e, col_max), i1 = min(col_base + col0 + 2 * e + 1, col_max);
+        dv = add2(dv, f2(-__ldg(drow + i0), -__ldg(drow + i1)));
+        gv = mul2(gv, f2(scale));
+      }
+      const f2_t ds = mul2(dv, gv);
+      dk[e] = pack16<C::DT>(f2_lo(ds), f2_hi(ds));
+    }
+    // dS^T row `row`, query columns col0..col0+31: box w, 16-byte chunks 4c..4c+3, XOR-swizzled by row
+    uint8_t* base = sDS + w * C::BOX_BYTES + row * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(base + (((4 * c + q) ^ (row & 7)) << 4)) =
+          make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
   }
 }
 
 template <class C, bool MASKED>
-__device__ __forceinline__ void bwd_tile_dispatch(int act, uint32_t t_lane, uint8_t* sDS, int row, int w,
-                                                  const BwdConsts& k, int c_lo, int c_hi, const float* lse,
-                                                  const float* drow, int col_base, int col_max) {
+__device__ __forceinline__ void bwd_pass1_dispatch(int act, uint32_t t_lane, int w, const BwdConsts& k, int c_lo,
+                                                   int c_hi, const float* lse, int col_base, int col_max) {
 #define GDPA_BWD_CASE(A) \
-  case A: bwd_tile<C, A, MASKED>(t_lane, sDS, row, w, k, c_lo, c_hi, lse, drow, col_base, col_max); break;
+  case A: bwd_pass1<C, A, MASKED>(t_lane, w, k, c_lo, c_hi, lse, col_base, col_max); break;
   switch (act) {
     GDPA_BWD_CASE(ACT_IDENTITY)
     GDPA_BWD_CASE(ACT_GELU)
@@ -213,7 +246,7 @@ __device__ __forceinline__ void bwd_tile_dispatch(int act, uint32_t t_lane, uint
     GDPA_BWD_CASE(ACT_LEAKY_RELU)
     GDPA_BWD_CASE(ACT_SILU)
     GDPA_BWD_CASE(ACT_HARDSWISH)
-    default: bwd_tile<C, ACT_SOFTMAX, MASKED>(t_lane, sDS, row, w, k, c_lo, c_hi, lse, drow, col_base, col_max);
+    default: bwd_pass1<C, ACT_SOFTMAX, MASKED>(t_lane, w, k, c_lo, c_hi, lse, col_base, col_max);
   }
 #undef GDPA_BWD_CASE
 }
@@ -249,11 +282,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sm.qd_empty[i], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.ds_full, 256);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.p_full, 128 * C::NG);
+    mbar_init(&sm.ds_full, 128 * C::NG);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 128);
     mbar_init(&sm.acc_full, 1);
-    mbar_init(&sm.acc_empty, 256);
+    mbar_init(&sm.acc_empty, 128 * C::NG);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -328,14 +363,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                      C::IDESC_S, k > 0);
         }
       };
-      auto issue_grads = [&](int st, bool acc) {
-        const uint32_t q = aQ + st * C::Q_BYTES, d = aDO + st * C::DO_BYTES;
+      auto issue_dv = [&](int st, bool acc) {  // dV += P^T dO (A = P^T from TMEM)
+        const uint32_t d = aDO + st * C::DO_BYTES;
 #pragma unroll
-        for (int k = 0; k < C::T_MMAS; ++k) {  // dV += P^T dO
-          const uint32_t a_t = tbase + C::T_S + 64 * (k / 4) + 8 * (k % 4);
-          mma_f16_ts(tbase + C::T_DV, a_t, sdesc_sw128(d + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DV,
-                     (acc || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < C::T_MMAS; ++k)
+          mma_f16_ts(tbase + C::T_DV, tbase + C::T_S + pt_col<C>(k), sdesc_sw128(d + k * 2048, C::BOX_BYTES, 1024),
+                     C::IDESC_DV, (acc || k > 0) ? 1u : 0u);
+      };
+      auto issue_dk_dq = [&](int st, bool acc) {
+        const uint32_t q = aQ + st * C::Q_BYTES;
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k) {  // dK += dS^T Q
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
@@ -343,12 +379,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                      sdesc_sw128(q + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DK, (acc || k > 0) ? 1u : 0u);
         }
 #pragma unroll
-        for (int k = 0; k < C::T_MMAS; ++k) {  // dQ = dS K
+        for (int k = 0; k < C::T_MMAS; ++k)  // dQ = dS K
           mma_f16_ss(tbase + C::T_DQ, sdesc_sw128(aDS + k * 2048, C::BOX_BYTES, 1024),
                      sdesc_sw128(aK + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DQ, k > 0);
-        }
       };
-      uint32_t kv_cnt = 0, qd_it = 0, ds_cnt = 0, dqe = 0, acce = 0;
+      // Per step: S^T | dP^T (pass 1 runs) | dV (pass 2 runs) | dK, dQ. S^T of
+      // the next step reuses the S^T columns after dV and pass 2 read them;
+      // dP^T reuses the dQ columns once the drain has read dQ.
+      uint32_t kv_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, dqe = 0, acce = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int pos = zigzag_pos(round, blockIdx.x, G);
@@ -356,53 +394,47 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const BwdItem it = bwd_decode(args, pos);
         if (it.nsteps == 0) continue;
         ok = mbar_wait(&sm.kv_full, kv_cnt++ & 1, abort_flag);
-        if (ok) ok = mbar_wait(&sm.qd_full[qd_it % 2], (qd_it / 2) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(qd_it % 2);
-        ok = mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dp(qd_it % 2);
-        mma_commit(&sm.s_full);
-        for (int s = 0; s < it.nsteps; ++s) {
+        for (int s = 0; s < it.nsteps && ok; ++s) {
           const int st = qd_it % 2;
-          ok = mbar_wait(&sm.ds_full, ds_cnt++ & 1, abort_flag);
+          ok = mbar_wait(&sm.qd_full[st], (qd_it / 2) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(st);
+          mma_commit(&sm.s_full);
+          ok = mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(st);
+          mma_commit(&sm.dp_full);
+          ok = mbar_wait(&sm.p_full, p_cnt++ & 1, abort_flag);
           if (ok && s == 0) ok = mbar_wait(&sm.acc_empty, (acce++ & 1) ^ 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          issue_grads(st, s > 0);
+          issue_dv(st, s > 0);
+          ok = mbar_wait(&sm.ds_full, ds_cnt++ & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dk_dq(st, s > 0);
           mma_commit(&sm.dq_full);
           mma_commit(&sm.qd_empty[st]);
           ++qd_it;
           if (s == it.nsteps - 1) {
             mma_commit(&sm.acc_full);
             mma_commit(&sm.kv_empty);
-          } else {
-            const int st2 = qd_it % 2;
-            ok = mbar_wait(&sm.qd_full[st2], (qd_it / 2) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(st2);
-            ok = mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_dp(st2);
-            mma_commit(&sm.s_full);
           }
         }
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= C::ACT_WARP0 && warp < C::DRAIN_WARP0) {
     // ------------------------------------------------ elementwise groups + dK/dV epilogue
-    const int w = (warp - 4) / 4;
+    const int w = (warp - C::ACT_WARP0) / 4;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // key row within the block
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     using T = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
     const bool softmax = args.act == ACT_SOFTMAX;
     const BwdConsts bwd_k = make_bwd_consts(args.scale);
-    uint32_t s_cnt = 0, acc_cnt = 0;
+    uint32_t s_cnt = 0, dp_cnt = 0, acc_cnt = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int pos = zigzag_pos(round, blockIdx.x, G);
@@ -410,13 +442,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const BwdItem it = bwd_decode(args, pos);
       const int kk = it.k0 + row;
       const bool row_valid = row < it.krows;
-      // this group stores dV (w = 0) or dK (w = 1) of the block
-      const int ncols = w == 0 ? C::DV : C::DQK;
-      T* dst = reinterpret_cast<T*>(w == 0 ? args.dv : args.dk) +
-               (static_cast<size_t>(it.k_start + kk) * pb.h_kv + it.g) * ncols;
+      // the epilogue splits the 32-column chunks of dV then dK round-robin over the groups
+      const size_t krow = static_cast<size_t>(it.k_start + kk) * pb.h_kv + it.g;
+      T* dv_row = reinterpret_cast<T*>(args.dv) + krow * C::DV;
+      T* dk_row = reinterpret_cast<T*>(args.dk) + krow * C::DQK;
+      constexpr int NCH = (C::DV + C::DQK) / 32;
       if (it.nsteps == 0) {
         if (row_valid)
-          for (int q4 = 0; q4 < ncols * 2 / 16; ++q4) reinterpret_cast<uint4*>(dst)[q4] = make_uint4(0, 0, 0, 0);
+          for (int ch = w; ch < NCH; ch += C::NG) {
+            T* d = ch < C::DV / 32 ? dv_row + ch * 32 : dk_row + (ch - C::DV / 32) * 32;
+            for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(d)[q4] = make_uint4(0, 0, 0, 0);
+          }
         continue;
       }
       int qmin = 1, qmax = 0;
@@ -435,13 +471,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const float* drow = softmax ? args.drow + static_cast<size_t>(h) * pb.total_q : nullptr;
         const int col_base = it.q_start + q0;
         const int col_max = pb.total_q - 1;
-        if (__all_sync(0xffffffffu, c_lo <= 64 * w && c_hi >= 64 * w + 63))
-          bwd_tile_dispatch<C, false>(args.act, t_lane, sDS, row, w, bwd_k, c_lo, c_hi, lse, drow, col_base,
-                                      col_max);
+        if (__all_sync(0xffffffffu, c_lo <= C::GCOLS * w && c_hi >= C::GCOLS * w + C::GCOLS - 1))
+          bwd_pass1_dispatch<C, false>(args.act, t_lane, w, bwd_k, c_lo, c_hi, lse, col_base, col_max);
         else
-          bwd_tile_dispatch<C, true>(args.act, t_lane, sDS, row, w, bwd_k, c_lo, c_hi, lse, drow, col_base,
-                                     col_max);
+          bwd_pass1_dispatch<C, true>(args.act, t_lane, w, bwd_k, c_lo, c_hi, lse, col_base, col_max);
         tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full);
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.dp_full, dp_cnt++ & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        if (softmax)
+          bwd_pass2<C, true>(t_lane, sDS, row, w, bwd_k.scale, drow, col_base, col_max);
+        else
+          bwd_pass2<C, false>(t_lane, sDS, row, w, bwd_k.scale, drow, col_base, col_max);
         fence_async_shared();
         tc_fence_before();
         mbar_arrive(&sm.ds_full);
@@ -450,17 +493,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, acc_cnt++ & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t t_acc = t_lane + (w == 0 ? C::T_DV : C::T_DK);
 #pragma unroll 1
-      for (int ch = 0; ch < ncols / 32; ++ch) {
+      for (int ch = w; ch < NCH; ch += C::NG) {
+        const bool is_dv = ch < C::DV / 32;
+        const int cc = is_dv ? ch * 32 : (ch - C::DV / 32) * 32;
         uint32_t o[32];
-        tmem_ld32(t_acc + ch * 32, o);
+        tmem_ld32(t_lane + (is_dv ? C::T_DV : C::T_DK) + cc, o);
         tmem_ld_wait(o);
         if (row_valid) {
           uint32_t wv[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) wv[e] = pack16<C::DT>(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+          uint4* d4 = reinterpret_cast<uint4*>((is_dv ? dv_row : dk_row) + cc);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) d4[q4] = make_uint4(wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
         }
@@ -468,7 +512,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tc_fence_before();
       mbar_arrive(&sm.acc_empty);
     }
-  } else if (warp >= 12) {
+  } else if (warp >= C::DRAIN_WARP0) {
     // ------------------------------------------------ dQ drain: TMEM -> fp32 atomics
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // query row within the tile

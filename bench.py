@@ -87,6 +87,21 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+# ---------------------------------------------------------------- cross-rank aggregation (replicas)
+
+def reduce_max(value: float, dist=None, device=None) -> float:
+    """Max of a per-rank value over all ranks (the slowest replica sets the time)."""
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_step: float, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job TFLOP/s: every replica runs `steps` steps of the same workload."""
+    return flops_per_step * steps * world / (slowest_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks during the timed region
 
 class ClockSampler:
@@ -315,12 +330,8 @@ def main():
     step_ms = sum(s.elapsed_time(e) for s, e in ev_step)
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev_main) / K
     bwd_ms = sum(e[2].elapsed_time(e[3]) for e in ev_main) / K
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms_max = float(t.item())
-    total_flops = (f_fwd + f_bwd) * K * world
-    value = total_flops / (step_ms_max * 1e-3) / 1e12
+    step_ms_max = reduce_max(step_ms, dist, dev)
+    value = replica_throughput(f_fwd + f_bwd, K, world, step_ms_max)
 
     # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -351,10 +362,8 @@ def main():
             evs[i][1].record()
         torch.cuda.synchronize()
         barrier()
-        e_ms = torch.tensor([sum(s.elapsed_time(e) for s, e in evs)], dtype=torch.float64, device=dev)
-        if dist is not None:
-            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-        e2e = {"value": (f_fwd + f_bwd) * ke * world / (float(e_ms.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in evs), dist, dev)
+        e2e = {"value": replica_throughput(f_fwd + f_bwd, ke, world, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:

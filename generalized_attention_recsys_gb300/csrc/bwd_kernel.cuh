@@ -370,57 +370,74 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           mma_f16_ts(tbase + C::T_DV, tbase + C::T_S + pt_col<C>(k), sdesc_sw128(d + k * 2048, C::BOX_BYTES, 1024),
                      C::IDESC_DV, (acc || k > 0) ? 1u : 0u);
       };
-      auto issue_dk_dq = [&](int st, bool acc) {
+      auto issue_dq_dk = [&](int st, bool acc) {
         const uint32_t q = aQ + st * C::Q_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::T_MMAS; ++k)  // dQ = dS K
+          mma_f16_ss(tbase + C::T_DQ, sdesc_sw128(aDS + k * 2048, C::BOX_BYTES, 1024),
+                     sdesc_sw128(aK + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DQ, k > 0);
+        mma_commit(&sm.dq_full);
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k) {  // dK += dS^T Q
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
           mma_f16_ss(tbase + C::T_DK, sdesc_sw128(aDS + off, 16, 1024),
                      sdesc_sw128(q + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DK, (acc || k > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int k = 0; k < C::T_MMAS; ++k)  // dQ = dS K
-          mma_f16_ss(tbase + C::T_DQ, sdesc_sw128(aDS + k * 2048, C::BOX_BYTES, 1024),
-                     sdesc_sw128(aK + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DQ, k > 0);
       };
-      // Per step: S^T | dP^T (pass 1 runs) | dV (pass 2 runs) | dK, dQ. S^T of
-      // the next step reuses the S^T columns after dV and pass 2 read them;
-      // dP^T reuses the dQ columns once the drain has read dQ.
+      // Issue order per item (steps t = 0..n-1):
+      //   S^T(0), dP^T(0), dV(0), then for each t:
+      //   S^T(t+1), dQ(t), dK(t), dP^T(t+1), dV(t+1)
+      // Pass 1 of step t+1 (needs S^T(t+1) only) overlaps dQ(t), dK(t) and
+      // dP^T(t+1); pass 2 overlaps dV. S^T(t+1) may overwrite P^T/G^T(t)
+      // because dV(t) was issued before it and pass 2(t) has finished; dQ
+      // goes first so that its drain overlaps dK, before dP^T(t+1) reuses
+      // the dQ columns; the commit after dP^T(t+1) also covers dQ(t) and
+      // dK(t), so pass 2(t+1) may overwrite the dS tile they read.
       uint32_t kv_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, dqe = 0, acce = 0;
       bool ok = true;
+      auto issue_s_at = [&](uint32_t it_idx) -> bool {
+        const int st = it_idx % 2;
+        if (!mbar_wait(&sm.qd_full[st], (it_idx / 2) & 1, abort_flag)) return false;
+        tc_fence_after();
+        issue_s(st);
+        mma_commit(&sm.s_full);
+        return true;
+      };
+      auto issue_dp_dv_at = [&](uint32_t it_idx, bool first) -> bool {
+        const int st = it_idx % 2;
+        if (!mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag)) return false;
+        tc_fence_after();
+        issue_dp(st);
+        mma_commit(&sm.dp_full);
+        if (!mbar_wait(&sm.p_full, p_cnt++ & 1, abort_flag)) return false;
+        if (first && !mbar_wait(&sm.acc_empty, (acce++ & 1) ^ 1, abort_flag)) return false;
+        tc_fence_after();
+        issue_dv(st, !first);
+        return true;
+      };
       for (int round = 0; ok; ++round) {
         const int pos = zigzag_pos(round, blockIdx.x, G);
         if (pos >= n_work) break;
         const BwdItem it = bwd_decode(args, pos);
         if (it.nsteps == 0) continue;
         ok = mbar_wait(&sm.kv_full, kv_cnt++ & 1, abort_flag);
+        if (ok) ok = issue_s_at(qd_it);
+        if (ok) ok = issue_dp_dv_at(qd_it, true);
         for (int s = 0; s < it.nsteps && ok; ++s) {
           const int st = qd_it % 2;
-          ok = mbar_wait(&sm.qd_full[st], (qd_it / 2) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(st);
-          mma_commit(&sm.s_full);
-          ok = mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dp(st);
-          mma_commit(&sm.dp_full);
-          ok = mbar_wait(&sm.p_full, p_cnt++ & 1, abort_flag);
-          if (ok && s == 0) ok = mbar_wait(&sm.acc_empty, (acce++ & 1) ^ 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dv(st, s > 0);
+          const bool more = s + 1 < it.nsteps;
           ok = mbar_wait(&sm.ds_full, ds_cnt++ & 1, abort_flag);
+          if (ok && more) ok = issue_s_at(qd_it + 1);
           if (!ok) break;
           tc_fence_after();
-          issue_dk_dq(st, s > 0);
-          mma_commit(&sm.dq_full);
+          issue_dq_dk(st, s > 0);
           mma_commit(&sm.qd_empty[st]);
           ++qd_it;
-          if (s == it.nsteps - 1) {
+          if (!more) {
             mma_commit(&sm.acc_full);
             mma_commit(&sm.kv_empty);
+          } else {
+            ok = issue_dp_dv_at(qd_it, false);
           }
         }
       }

@@ -89,6 +89,25 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int heads, int dim, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows, heads, dim] accumulator as the target of TMA reduce-adds: boxes
+// of 32 rows x 32 columns (128 bytes, the 128-byte swizzle span).
+bool make_acc_map(CUtensorMap* m, float* ptr, int rows, int heads, int dim, const void* fallback) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  void* base = ptr;
+  if (rows <= 0 || ptr == nullptr) {
+    rows = 1;
+    base = const_cast<void*>(fallback);
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 4, static_cast<cuuint64_t>(heads) * dim * 4};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -326,13 +345,14 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.d_qk = s->d_qk;
   a.d_v = s->d_v;
   a.dtype = s->dtype;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_map(&tq, q, s->total_q, s->h_q, s->d_qk, s->dtype, workspace) ||
       !make_map(&tk, k, s->total_k, s->h_kv, s->d_qk, s->dtype, workspace) ||
       !make_map(&tv, v, s->total_k, s->h_kv, s->d_v, s->dtype, workspace) ||
-      !make_map(&tdo, dout, s->total_q, s->h_q, s->d_v, s->dtype, workspace))
+      !make_map(&tdo, dout, s->total_q, s->h_q, s->d_v, s->dtype, workspace) ||
+      !make_acc_map(&tdq, dq_acc, s->total_q, s->h_q, s->d_qk, workspace))
     return GDPA_ERR_CUDA;
-  const cudaError_t e = launch_bwd(tq, tk, tv, tdo, a, nsm, stream, t_ev_before, t_ev_after);
+  const cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, a, nsm, stream, t_ev_before, t_ev_after);
   return e == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 

@@ -49,7 +49,7 @@ cudaError_t launch_fwd_d192(int dtype, const CUtensorMap& tq, const CUtensorMap&
 // kernel, and the dQ conversion, all on `stream`.
 // `before`/`after` (may be NULL) are recorded around the main kernel only.
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid, cudaStream_t stream,
                        cudaEvent_t before, cudaEvent_t after);
 
 }  // namespace gdpa

@@ -8,11 +8,14 @@
 namespace gdpa {
 
 cudaError_t launch_bwd_d64(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_bwd_d96(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_bwd_d128(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                           cudaStream_t stream);
 
 namespace {
 
@@ -73,7 +76,8 @@ __global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T*
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdArgs& a, int grid, cudaStream_t stream, cudaEvent_t before, cudaEvent_t after) {
+                       const CUtensorMap& tdq, const BwdArgs& a, int grid, cudaStream_t stream, cudaEvent_t before,
+                       cudaEvent_t after) {
   const size_t n4 = static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4;
   const int eg = grid * 8;  // elementwise kernels: 8 blocks of 256 per SM
   float* drow = a.act == 9 ? a.drow : nullptr;
@@ -89,9 +93,9 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (e != cudaSuccess) return e;
   if (before) cudaEventRecord(before, stream);
   switch (a.d_qk) {
-    case 64: e = launch_bwd_d64(a.dtype, tq, tk, tv, tdo, a, grid, stream); break;
-    case 96: e = launch_bwd_d96(a.dtype, tq, tk, tv, tdo, a, grid, stream); break;
-    case 128: e = launch_bwd_d128(a.dtype, tq, tk, tv, tdo, a, grid, stream); break;
+    case 64: e = launch_bwd_d64(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
+    case 96: e = launch_bwd_d96(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
+    case 128: e = launch_bwd_d128(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
     default: return cudaErrorNotSupported;
   }
   if (e != cudaSuccess) return e;

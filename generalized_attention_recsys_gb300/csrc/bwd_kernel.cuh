@@ -12,8 +12,8 @@
 // in shared memory while the CTA walks every query head of the kv head's
 // group and every 128-row query block that sees the key block, so dK and dV
 // accumulate in TMEM without atomics (GQA/MQA heads summed in place). dQ is
-// reduced across key blocks with fp32 vector atomics into a workspace and
-// converted at the end.
+// reduced across key blocks into an fp32 workspace with TMA bulk tensor
+// reduce-adds (one 32 x 32 box per warp and chunk) and converted at the end.
 //
 // All products are computed transposed so that TMEM lanes are key rows:
 //   S^T  = K Q^T      (A = K   smem K-major,  B = Q   smem K-major)
@@ -24,9 +24,13 @@
 // TMEM (512 columns): S^T [0,128) with P^T written over it, dP^T [128,256)
 // reused for dQ once dP^T has been read, dV [256,256+dv), dK [384,384+dqk).
 //
-// Warp roles (128 * (NG + 2) threads): warp 0 TMA, warp 1 MMA, NG elementwise
-// groups of four warps (128 / NG query columns of each tile each), then four
-// warps that drain dQ from TMEM into the fp32 accumulator.
+// Warp roles (128 * (NG + 2) threads): warp 0 TMA for K/V, warp 1 MMA,
+// warp 2 TMA for Q, warp 3 TMA for dO, NG elementwise groups of four warps
+// (128 / NG query columns of each tile each), then four warps that drain dQ
+// from TMEM into the fp32 accumulator.
+//
+// Shared memory: K, V, two Q stages, one dO stage, the dS^T tile and the dQ
+// staging ring (d = 128: 32 + 32 + 64 + 32 + 32 + 32 KB).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -55,10 +59,12 @@ struct BwdCfg {
   static constexpr int Q_BYTES = K_BYTES;
   static constexpr int DO_BYTES = V_BYTES;
   static constexpr int DS_BYTES = 2 * BOX_BYTES;
-  static constexpr int STAGES = 2;
+  static constexpr int Q_STAGES = 2;  // dO is single-buffered: its next tile loads while S^T, dQ, dK run
+  static constexpr int DQ_CHUNK_BYTES = 32 * 128;              // 32 query rows x 32 fp32 columns
+  static constexpr int DQ_STAGE_BYTES = 4 * 2 * DQ_CHUNK_BYTES;  // per drain warp: a ring of two chunks
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES =
-      1024 + K_BYTES + V_BYTES + STAGES * (Q_BYTES + DO_BYTES) + DS_BYTES + BAR_BYTES;
+      1024 + K_BYTES + V_BYTES + Q_STAGES * Q_BYTES + DO_BYTES + DS_BYTES + DQ_STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "tiles do not fit in shared memory");
   static constexpr int K_STEP = 16;
   static constexpr int S_MMAS = DQK / K_STEP;
@@ -116,16 +122,11 @@ __device__ __forceinline__ void bwd_step(const BwdItem& it, const Problem& pb, i
 
 struct BwdSmem {
   uint64_t kv_full, kv_empty;
-  uint64_t qd_full[2], qd_empty[2];
+  uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_full, acc_empty;
   uint32_t tmem_base;
   int abort_flag;
 };
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 template <int DT>
 __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
@@ -255,15 +256,16 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     gdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdArgs args) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::K_BYTES;
-  uint8_t* sQ = sV + C::V_BYTES;                    // STAGES x Q_BYTES
-  uint8_t* sDO = sQ + C::STAGES * C::Q_BYTES;       // STAGES x DO_BYTES
-  uint8_t* sDS = sDO + C::STAGES * C::DO_BYTES;     // 128 key rows x 128 query columns
-  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(sDS + C::DS_BYTES);
+  uint8_t* sQ = sV + C::V_BYTES;                 // Q_STAGES x Q_BYTES
+  uint8_t* sDO = sQ + C::Q_STAGES * C::Q_BYTES;  // one dO tile
+  uint8_t* sDS = sDO + C::DO_BYTES;              // 128 key rows x 128 query columns
+  uint8_t* sDQ = sDS + C::DS_BYTES;              // dQ staging for the TMA reduce-adds
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(sDQ + C::DQ_STAGE_BYTES);
   static_assert(sizeof(BwdSmem) <= C::BAR_BYTES, "barrier block too large");
 
   const int warp = threadIdx.x / 32;
@@ -278,9 +280,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.qd_full[i], 1);
-      mbar_init(&sm.qd_empty[i], 1);
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 1);
     }
+    mbar_init(&sm.do_full, 1);
+    mbar_init(&sm.do_empty, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
     mbar_init(&sm.p_full, 128 * C::NG);
@@ -300,43 +304,54 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------------------------ TMA producers
+    // warp 0 loads each item's K and V, warp 2 streams the Q tile and warp 3
+    // the dO tile of every step, so the next item's first tiles load while
+    // the current item still holds K and V.
     if (lane == 0) {
-      uint32_t kv_cnt = 0, qd_it = 0;
+      uint32_t kv_cnt = 0, st_it = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int pos = zigzag_pos(round, blockIdx.x, G);
         if (pos >= n_work) break;
         const BwdItem it = bwd_decode(args, pos);
         if (it.nsteps == 0) continue;
-        ok = mbar_wait(&sm.kv_empty, (kv_cnt++ & 1) ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&sm.kv_full, C::K_BYTES + C::V_BYTES);
-        for (int bx = 0; bx < C::QK_BOXES; ++bx)
-          tma_load_3d(sK + bx * C::BOX_BYTES, &tm_k, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
-        for (int bx = 0; bx < C::V_BOXES; ++bx)
-          tma_load_3d(sV + bx * C::BOX_BYTES, &tm_v, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
-        for (int s = 0; s < it.nsteps && ok; ++s) {
+        if (warp == 0) {
+          ok = mbar_wait(&sm.kv_empty, (kv_cnt++ & 1) ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&sm.kv_full, C::K_BYTES + C::V_BYTES);
+          for (int bx = 0; bx < C::QK_BOXES; ++bx)
+            tma_load_3d(sK + bx * C::BOX_BYTES, &tm_k, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
+          for (int bx = 0; bx < C::V_BOXES; ++bx)
+            tma_load_3d(sV + bx * C::BOX_BYTES, &tm_v, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
+          continue;
+        }
+        for (int s = 0; s < it.nsteps && ok; ++s, ++st_it) {
           int h, q0;
           bwd_step(it, pb, s, h, q0);
-          const int st = qd_it % 2;
-          ok = mbar_wait(&sm.qd_empty[st], ((qd_it / 2) & 1) ^ 1, abort_flag);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&sm.qd_full[st], C::Q_BYTES + C::DO_BYTES);
-          for (int bx = 0; bx < C::QK_BOXES; ++bx)
-            tma_load_3d(sQ + st * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.qd_full[st], bx * 64, h,
-                        it.q_start + q0);
-          for (int bx = 0; bx < C::V_BOXES; ++bx)
-            tma_load_3d(sDO + st * C::DO_BYTES + bx * C::BOX_BYTES, &tm_do, &sm.qd_full[st], bx * 64, h,
-                        it.q_start + q0);
-          ++qd_it;
+          if (warp == 2) {
+            const int st = st_it % C::Q_STAGES;
+            ok = mbar_wait(&sm.q_empty[st], ((st_it / C::Q_STAGES) & 1) ^ 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&sm.q_full[st], C::Q_BYTES);
+            for (int bx = 0; bx < C::QK_BOXES; ++bx)
+              tma_load_3d(sQ + st * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[st], bx * 64, h,
+                          it.q_start + q0);
+          } else {
+            ok = mbar_wait(&sm.do_empty, (st_it & 1) ^ 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&sm.do_full, C::DO_BYTES);
+            for (int bx = 0; bx < C::V_BOXES; ++bx)
+              tma_load_3d(sDO + bx * C::BOX_BYTES, &tm_do, &sm.do_full, bx * 64, h, it.q_start + q0);
+          }
         }
       }
     }
@@ -354,8 +369,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                      k > 0);
         }
       };
-      auto issue_dp = [&](int st) {
-        const uint32_t d = aDO + st * C::DO_BYTES;
+      auto issue_dp = [&]() {
+        const uint32_t d = aDO;
 #pragma unroll
         for (int k = 0; k < C::DP_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
@@ -363,8 +378,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                      C::IDESC_S, k > 0);
         }
       };
-      auto issue_dv = [&](int st, bool acc) {  // dV += P^T dO (A = P^T from TMEM)
-        const uint32_t d = aDO + st * C::DO_BYTES;
+      auto issue_dv = [&](bool acc) {  // dV += P^T dO (A = P^T from TMEM)
+        const uint32_t d = aDO;
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k)
           mma_f16_ts(tbase + C::T_DV, tbase + C::T_S + pt_col<C>(k), sdesc_sw128(d + k * 2048, C::BOX_BYTES, 1024),
@@ -396,23 +411,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t kv_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, dqe = 0, acce = 0;
       bool ok = true;
       auto issue_s_at = [&](uint32_t it_idx) -> bool {
-        const int st = it_idx % 2;
-        if (!mbar_wait(&sm.qd_full[st], (it_idx / 2) & 1, abort_flag)) return false;
+        const int st = it_idx % C::Q_STAGES;
+        if (!mbar_wait(&sm.q_full[st], (it_idx / C::Q_STAGES) & 1, abort_flag)) return false;
         tc_fence_after();
         issue_s(st);
         mma_commit(&sm.s_full);
         return true;
       };
       auto issue_dp_dv_at = [&](uint32_t it_idx, bool first) -> bool {
-        const int st = it_idx % 2;
         if (!mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag)) return false;
+        if (!mbar_wait(&sm.do_full, it_idx & 1, abort_flag)) return false;
         tc_fence_after();
-        issue_dp(st);
+        issue_dp();
         mma_commit(&sm.dp_full);
         if (!mbar_wait(&sm.p_full, p_cnt++ & 1, abort_flag)) return false;
         if (first && !mbar_wait(&sm.acc_empty, (acce++ & 1) ^ 1, abort_flag)) return false;
         tc_fence_after();
-        issue_dv(st, !first);
+        issue_dv(!first);
+        mma_commit(&sm.do_empty);  // dV is the last reader of this dO tile
         return true;
       };
       for (int round = 0; ok; ++round) {
@@ -424,14 +440,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (ok) ok = issue_s_at(qd_it);
         if (ok) ok = issue_dp_dv_at(qd_it, true);
         for (int s = 0; s < it.nsteps && ok; ++s) {
-          const int st = qd_it % 2;
+          const int st = qd_it % C::Q_STAGES;
           const bool more = s + 1 < it.nsteps;
           ok = mbar_wait(&sm.ds_full, ds_cnt++ & 1, abort_flag);
           if (ok && more) ok = issue_s_at(qd_it + 1);
           if (!ok) break;
           tc_fence_after();
           issue_dq_dk(st, s > 0);
-          mma_commit(&sm.qd_empty[st]);
+          mma_commit(&sm.q_empty[st]);
           ++qd_it;
           if (!more) {
             mma_commit(&sm.acc_full);
@@ -530,11 +546,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_arrive(&sm.acc_empty);
     }
   } else if (warp >= C::DRAIN_WARP0) {
-    // ------------------------------------------------ dQ drain: TMEM -> fp32 atomics
+    // ------------------------------------------------ dQ drain: TMEM -> smem -> TMA reduce-add
+    // Each warp owns 32 query rows (its TMEM lane quadrant). Per 32-column
+    // chunk it stages a 32 x 32 fp32 box in shared memory (128-byte swizzle)
+    // and lane 0 adds it into the fp32 accumulator with one bulk tensor
+    // reduce; a ring of two boxes per warp lets the next chunk's TMEM read
+    // overlap the previous reduce. Rows past the sequence end are staged as
+    // zeros, so adding them into the next sequence's rows changes nothing.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // query row within the tile
     const uint32_t t_dq = tbase + (static_cast<uint32_t>(quad * 32) << 16) + C::T_DQ;
-    uint32_t dq_cnt = 0;
+    uint8_t* stage = sDQ + quad * 2 * C::DQ_CHUNK_BYTES;
+    uint32_t dq_cnt = 0, chunk_it = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int pos = zigzag_pos(round, blockIdx.x, G);
@@ -543,28 +566,38 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int s = 0; s < it.nsteps; ++s) {
         int h, q0;
         bwd_step(it, pb, s, h, q0);
-        const int qq = q0 + row;
-        const bool valid = qq < it.lq;
-        float* dst = args.dq_acc + (static_cast<size_t>(it.q_start + qq) * pb.h_q + h) * C::DQK;
+        const bool valid = q0 + row < it.lq;
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_full, dq_cnt++ & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < C::DQK / 32; ++ch) {
+        for (int ch = 0; ch < C::DQK / 32; ++ch, ++chunk_it) {
           uint32_t o[32];
           tmem_ld32(t_dq + ch * 32, o);
+          if (ch == C::DQK / 32 - 1) {
+            tmem_ld_wait(o);
+            tc_fence_before();
+            mbar_arrive(&sm.dq_empty);  // every TMEM read of this tile is done
+          }
+          uint8_t* box = stage + (chunk_it & 1) * C::DQ_CHUNK_BYTES;
+          if (lane == 0) bulk_wait_group_read<1>();  // the reduce that last read this box is done with it
+          __syncwarp();
           tmem_ld_wait(o);
-          if (valid) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              red_add_v4(dst + ch * 32 + 4 * i, __uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                         __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = valid ? make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+          }
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0 && q0 + quad * 32 < it.lq) {  // skip boxes that lie wholly past the sequence
+            tma_reduce_add_3d(&tm_dq, box, ch * 32, h, it.q_start + q0 + quad * 32);
+            bulk_commit_group();
           }
         }
-        tc_fence_before();
-        mbar_arrive(&sm.dq_empty);
       }
     }
+    if (lane == 0) bulk_wait_group_all();
   }
 
   // ------------------------------------------------ teardown
@@ -586,12 +619,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
 template <int DQK, int DV, int DT>
 cudaError_t launch_bwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                           cudaStream_t stream) {
   using C = BwdCfg<DQK, DV, DT>;
   auto kern = gdpa_bwd_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 

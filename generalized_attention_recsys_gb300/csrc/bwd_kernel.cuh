@@ -570,6 +570,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_full, dq_cnt++ & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
+        if (q0 + quad * 32 >= it.lq) {  // this warp's 32 rows lie wholly past the sequence: nothing to add
+          tc_fence_before();
+          mbar_arrive(&sm.dq_empty);
+          continue;
+        }
+        // every staged chunk commits one bulk group, so the ring's box parity
+        // and the group count stay in step
 #pragma unroll 1
         for (int ch = 0; ch < C::DQK / 32; ++ch, ++chunk_it) {
           uint32_t o[32];
@@ -590,7 +597,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           fence_async_shared();
           __syncwarp();
-          if (lane == 0 && q0 + quad * 32 < it.lq) {  // skip boxes that lie wholly past the sequence
+          if (lane == 0) {
             tma_reduce_add_3d(&tm_dq, box, ch * 32, h, it.q_start + q0 + quad * 32);
             bulk_commit_group();
           }

@@ -169,7 +169,7 @@ __device__ __forceinline__ void bwd_pass1(uint32_t t_lane, int w, const BwdConst
         pv = f2(ex2_approx(f2_lo(a)), ex2_approx(f2_hi(a)));
         gv = pv;
       } else {
-        act_pair_grad<ACT>(sv, f2(1.0f), k, pv, gv);
+        act_pair_grad<ACT>(sv, k, pv, gv);
       }
       float p0 = f2_lo(pv), p1 = f2_hi(pv), g0 = f2_lo(gv), g1 = f2_hi(gv);
       if (MASKED) {

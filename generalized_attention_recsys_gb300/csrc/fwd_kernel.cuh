@@ -11,19 +11,23 @@
 // same flattened stream of steps across items. Warp roles (512 threads):
 //   warp 0       TMA producer: Q tiles (one item ahead, double-buffered) and
 //                a K/V ring
-//   warp 1       MMA issuer (one thread)
+//   warp 1       MMA issuer for S = Q K^T (one thread)
+//   warp 2       MMA issuer for O += P V (one thread)
 //   warps 4-7    activation group 0: score columns 0-63 of every S tile
 //   warps 8-11   activation group 1: score columns 64-127
 //   warps 12-15  epilogue: O from TMEM to global memory (softmax: O / l, lse)
 // TMEM (512 columns): S buffers [0,128) and [128,256), P buffers [256,320)
 // and [320,384) (bf16/f16 pairs or e4m3 quads per column), O [384,384+dv).
 //
-// Because P has its own buffers, S of step u+2 can be computed into S
-// buffer u%2 as soon as the activation groups have read S of step u: the
-// tensor core runs PV(u) and S(u+2) while the groups work on S(u+1), so
-// activation latency hides behind two GEMMs instead of sitting between them.
-// tcgen05.mma executes in issue order, so a commit after S(u+2) also covers
-// PV(u), which frees P buffer u%2 before step u+2's activation overwrites it.
+// Two issuing threads: one tcgen05.mma costs its issuing thread about as
+// long as an N=128 MMA takes to execute, and every barrier wait or commit
+// on a single issuer leaves the tensor core idle. With S and PV issued from
+// different warps, one issuer's waits overlap the other's MMAs. Because P
+// has its own buffers, S of step u+2 is computed into S buffer u%2 as soon
+// as the activation groups have read S of step u (signalled by P(u) being
+// full), so activation latency hides behind the GEMMs. The two streams are
+// not ordered against each other, so the activation groups wait for
+// pv_done[u%2] (PV(u-2) has read P buffer u%2) before storing P(u).
 //
 // Short KV ("Outer-loop software pipelining for short K/V sequences",
 // Features): the step stream crosses item boundaries, so with one or two KV
@@ -150,7 +154,7 @@ struct FwdSmem {
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_full, o_empty, pv_done;
+  uint64_t o_full, o_empty, pv_done[2];
   uint64_t stat_full, stat_empty;
   uint32_t tmem_base;
   int abort_flag;
@@ -161,19 +165,49 @@ struct FwdSmem {
 
 // ---------------------------------------------------------------- activation groups
 
-// Converts 32 floats to the P storage type and writes them to TMEM.
+// P buffer u % 2 last held P(u - 2); the PV issuer signals pv_done[u % 2]
+// once PV(u - 2) has read it. Who waits for that depends on the activation
+// (pv_gate_on_s below): for costly activations the S issuer waits before
+// issuing S(u), which keeps the poll off the activation warps' critical
+// path; for cheap ones the activation warps wait just before their first
+// store, so S(u) is not held back.
+__host__ __device__ constexpr bool pv_gate_on_s(int act) {
+  return act == ACT_GELU || act == ACT_GELU_TANH || act == ACT_SILU || act == ACT_SOFTMAX;
+}
+
+struct StepSync {
+  uint64_t* pv_done;
+  uint32_t u;
+  volatile int* abort_flag;
+  bool gated;  // the S issuer already waited for PV(u-2) before issuing S(u)
+  __device__ __forceinline__ bool wait_p_buffer() const {
+    if (u < 2 || gated) return true;
+    return __all_sync(0xffffffffu, mbar_wait(pv_done, ((u - 2) >> 1) & 1, abort_flag));
+  }
+};
+
+// Packs 32 floats into the P storage type (16 words of bf16/f16 pairs or 8
+// words of e4m3 quads).
 template <int DT>
-__device__ __forceinline__ void store_p_chunk(uint32_t taddr, const float (&p)[32]) {
+__device__ __forceinline__ void pack_p_chunk(const float (&p)[32], uint32_t (&r)[16]) {
   if constexpr (DT == DT_E4M3) {
-    uint32_t r[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) r[i] = pack_e4m3x4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-    tmem_st8(taddr, r);
   } else {
-    uint32_t r[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
       r[i] = DT == DT_BF16 ? pack_bf16x2(p[2 * i], p[2 * i + 1]) : pack_f16x2(p[2 * i], p[2 * i + 1]);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void store_p_chunk(uint32_t taddr, const uint32_t (&r)[16]) {
+  if constexpr (DT == DT_E4M3) {
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = r[i];
+    tmem_st8(taddr, q);
+  } else {
     tmem_st16(taddr, r);
   }
 }
@@ -182,8 +216,8 @@ __device__ __forceinline__ void store_p_chunk(uint32_t taddr, const float (&p)[3
 // columns of an S tile; thread = one row (TMEM lane). t_s / t_p: this lane's
 // address of the group's first S / P column; col0 = 64 * group.
 template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ void act_half(uint32_t t_s, uint32_t t_p, int col0, const ActConsts& k, int c_lo,
-                                         int c_hi) {
+__device__ __forceinline__ bool act_half(uint32_t t_s, uint32_t t_p, int col0, const ActConsts& k, int c_lo,
+                                         int c_hi, const StepSync& sync) {
   uint32_t sa[32], sb[32];
   tmem_ld32(t_s, sa);
   tmem_ld32(t_s + 32, sb);
@@ -205,23 +239,27 @@ __device__ __forceinline__ void act_half(uint32_t t_s, uint32_t t_p, int col0, c
       p[2 * e] = v0;
       p[2 * e + 1] = v1;
     }
-    store_p_chunk<C::DT>(t_p + ch * C::P_COLS_PER_32, p);
+    uint32_t pk[16];
+    pack_p_chunk<C::DT>(p, pk);
+    if (ch == 0 && !sync.wait_p_buffer()) return false;  // first store into the buffer
+    store_p_chunk<C::DT>(t_p + ch * C::P_COLS_PER_32, pk);
   }
+  return true;
 }
 
 template <class C, bool MASKED>
-__device__ __forceinline__ void act_half_dispatch(int act, uint32_t t_s, uint32_t t_p, int col0,
-                                                  const ActConsts& k, int c_lo, int c_hi) {
+__device__ __forceinline__ bool act_half_dispatch(int act, uint32_t t_s, uint32_t t_p, int col0, const ActConsts& k,
+                                                  int c_lo, int c_hi, const StepSync& sync) {
   switch (act) {
-    case ACT_IDENTITY: act_half<C, ACT_IDENTITY, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_GELU: act_half<C, ACT_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_GELU_TANH: act_half<C, ACT_GELU_TANH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_FAST_GELU: act_half<C, ACT_FAST_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_RELU: act_half<C, ACT_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_RELU2: act_half<C, ACT_RELU2, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_LEAKY_RELU: act_half<C, ACT_LEAKY_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    case ACT_SILU: act_half<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
-    default: act_half<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi); break;
+    case ACT_IDENTITY: return act_half<C, ACT_IDENTITY, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_GELU: return act_half<C, ACT_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_GELU_TANH: return act_half<C, ACT_GELU_TANH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_FAST_GELU: return act_half<C, ACT_FAST_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_RELU: return act_half<C, ACT_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_RELU2: return act_half<C, ACT_RELU2, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_LEAKY_RELU: return act_half<C, ACT_LEAKY_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_SILU: return act_half<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    default: return act_half<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
   }
 }
 
@@ -267,7 +305,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_empty, 128);
-    mbar_init(&sm.pv_done, 1);
+    mbar_init(&sm.pv_done[0], 1);
+    mbar_init(&sm.pv_done[1], 1);
     mbar_init(&sm.stat_full, 256);
     mbar_init(&sm.stat_empty, 128);
     fence_mbar_init();
@@ -334,26 +373,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer: S = Q K^T
     if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-      uint32_t k_it = 0, v_it = 0, s_step = 0, pv_step = 0, o_cnt = 0;
-      StepCursor sc, pc;  // sc: next S to issue (two steps ahead of pc), pc: next PV
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK);
+      uint32_t k_it = 0, u = 0;
+      const bool gate = pv_gate_on_s(args.act);
+      StepCursor sc;
       sc.start(args, n_work);
-      pc.start(args, n_work);
       bool ok = true;
-      auto issue_s = [&]() {
+      while (sc.active && ok) {
         const int slot = sc.item_idx % C::QST;
-        if (sc.j == sc.it.lo) {
-          ok = mbar_wait(&sm.q_full[slot], (sc.item_idx / C::QST) & 1, abort_flag);
-          if (!ok) return;
+        const int b = u & 1;
+        // S buffer b last held S(u-2): the activation groups have read it once P(u-2) is full
+        if (u >= 2) {
+          ok = mbar_wait(&sm.p_full[b], ((u - 2) >> 1) & 1, abort_flag);
+          if (ok && gate) ok = mbar_wait(&sm.pv_done[b], ((u - 2) >> 1) & 1, abort_flag);
         }
+        if (ok && sc.j == sc.it.lo) ok = mbar_wait(&sm.q_full[slot], (sc.item_idx / C::QST) & 1, abort_flag);
         const int ks = k_it % C::KST;
-        ok = mbar_wait(&sm.k_full[ks], (k_it / C::KST) & 1, abort_flag);
-        if (!ok) return;
+        if (ok) ok = mbar_wait(&sm.k_full[ks], (k_it / C::KST) & 1, abort_flag);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t a0 = sQa + slot * C::Q_BYTES, b0 = sKa + ks * C::K_BYTES;
-        const uint32_t d = tbase + C::T_S + (s_step & 1) * 128;
+        const uint32_t d = tbase + C::T_S + b * 128;
 #pragma unroll
         for (int k = 0; k < C::S_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
@@ -362,17 +404,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           else
             mma_f16_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::IDESC_S, k > 0);
         }
-        mma_commit(&sm.s_full[s_step & 1]);
+        mma_commit(&sm.s_full[b]);
         mma_commit(&sm.k_empty[ks]);
         ++k_it;
         if (sc.j == sc.it.hi) mma_commit(&sm.q_empty[slot]);
-        ++s_step;
+        ++u;
         sc.advance(args, n_work);
-      };
-      for (int i = 0; i < 2 && sc.active && ok; ++i) issue_s();
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------ MMA issuer: O += P V
+    if (lane == 0) {
+      const uint32_t sVa = smem_u32(sV);
+      uint32_t v_it = 0, u = 0, o_cnt = 0;
+      StepCursor pc;
+      pc.start(args, n_work);
+      bool ok = true;
       while (pc.active && ok) {
-        const int b = pv_step & 1;
-        ok = mbar_wait(&sm.p_full[b], (pv_step >> 1) & 1, abort_flag);
+        const int b = u & 1;
+        ok = mbar_wait(&sm.p_full[b], (u >> 1) & 1, abort_flag);
         if (ok && pc.j == pc.it.lo) ok = mbar_wait(&sm.o_empty, (o_cnt++ & 1) ^ 1, abort_flag);
         const int vs = v_it % C::VST;
         if (ok) ok = mbar_wait(&sm.v_full[vs], (v_it / C::VST) & 1, abort_flag);
@@ -390,12 +440,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mma_f16_ts(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
         }
         mma_commit(&sm.v_empty[vs]);
-        mma_commit(&sm.pv_done);
+        mma_commit(&sm.pv_done[b]);
         ++v_it;
         if (pc.j == pc.it.hi) mma_commit(&sm.o_full);
-        ++pv_step;
+        ++u;
         pc.advance(args, n_work);
-        if (sc.active) issue_s();
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -430,11 +479,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int c_lo = kmin - j * kTileK, c_hi = kmax - j * kTileK;
         const uint32_t t_s = t_lane + C::T_S + b * 128 + col0;
         const uint32_t t_p = t_lane + C::T_P + b * 64 + grp * (2 * C::P_COLS_PER_32);
+        const StepSync sync{&sm.pv_done[b], u, abort_flag, pv_gate_on_s(args.act)};
         if (!softmax) {
           if (__all_sync(0xffffffffu, c_lo <= col0 && c_hi >= col0 + 63))
-            act_half_dispatch<C, false>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi);
+            ok = act_half_dispatch<C, false>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
           else
-            act_half_dispatch<C, true>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi);
+            ok = act_half_dispatch<C, true>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
+          if (!ok) break;
         } else {
           // online softmax in the log2 domain; both groups agree on the row max
           uint32_t sa[32], sb[32];
@@ -458,7 +509,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const float alpha = raise && m != -INFINITY ? ex2_approx(m - m_new) : 1.0f;
           if (__any_sync(0xffffffffu, raise && m != -INFINITY) && j > it.lo) {
             // O holds the previous step's PV: wait for it, then rescale this group's half of O
-            ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (u - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_o = t_lane + C::T_O + grp * (C::DV / 2);
@@ -487,6 +538,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           l *= alpha;
           m = m_new;
+          ok = sync.wait_p_buffer();
+          if (!ok) break;
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t(&cur)[32] = ch ? sb : sa;
@@ -498,7 +551,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               l += v;
               p[e] = v;
             }
-            store_p_chunk<C::DT>(t_p + ch * C::P_COLS_PER_32, p);
+            uint32_t pk[16];
+            pack_p_chunk<C::DT>(p, pk);
+            store_p_chunk<C::DT>(t_p + ch * C::P_COLS_PER_32, pk);
           }
         }
         tmem_st_wait();

@@ -8,14 +8,20 @@
 // One persistent CTA per SM walks a cost-sorted work list in zigzag order
 // ("Zigzag tile scheduling", Features). A work item is one 128-row Q tile of
 // one (sequence, head); its KV blocks form "steps", and all roles walk the
-// same flattened stream of steps across items. Warp roles (512 threads):
+// same flattened stream of steps across items. Warp roles (128 + 128 NG
+// threads, NG = 2 or 4 activation groups):
 //   warp 0       TMA producer: Q tiles (one item ahead, double-buffered) and
 //                a K/V ring
 //   warp 1       MMA issuer for S = Q K^T (one thread)
 //   warp 2       MMA issuer for O += P V (one thread)
-//   warps 4-7    activation group 0: score columns 0-63 of every S tile
-//   warps 8-11   activation group 1: score columns 64-127
-//   warps 12-15  epilogue: O from TMEM to global memory (softmax: O / l, lse)
+//   warps 4..    NG activation groups of four warps (one per TMEM lane
+//                quadrant); group g owns score columns [g 128/NG, +128/NG)
+//                of every S tile and, at the end of an item, O columns
+//                [g dv/NG, +dv/NG) (softmax: O / l and lse)
+// Four groups (sixteen warps, four per SM sub-partition) keep the FMA pipes
+// fed where the activation's arithmetic sets the pace; two leave each thread
+// more registers elsewhere. The epilogue of an item runs after the next
+// item's first step, so the item's last PV has finished by then.
 // TMEM (512 columns): S buffers [0,128) and [128,256), P buffers [256,320)
 // and [320,384) (bf16/f16 pairs or e4m3 quads per column), O [384,384+dv).
 //
@@ -48,9 +54,9 @@
 
 namespace gdpa {
 
-template <int DQK_, int DV_, int DT_>
+template <int DQK_, int DV_, int DT_, int NG_>
 struct FwdCfg {
-  static constexpr int DQK = DQK_, DV = DV_, DT = DT_;
+  static constexpr int DQK = DQK_, DV = DV_, DT = DT_, NG = NG_;
   static constexpr int ESZ = DT == DT_E4M3 ? 1 : 2;
   static constexpr int BOX_ELEMS = 128 / ESZ;  // elements per 128-byte swizzle row
   static constexpr int BOX_BYTES = 128 * 128;  // one 128-row x 128-byte swizzled box
@@ -60,7 +66,7 @@ struct FwdCfg {
   static constexpr int K_BYTES = QK_BOXES * BOX_BYTES;
   static constexpr int V_BYTES = V_BOXES * BOX_BYTES;
   static constexpr int SMEM_LIMIT = 232448;  // 227 KB per block
-  static constexpr int EXTRA_BYTES = 4608;   // barriers + softmax row exchange
+  static constexpr int EXTRA_BYTES = 7168;   // barriers + softmax row exchange
   static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES;
   // Q double-buffered when two K/V stages still fit, else single
   static constexpr int QST = (AVAIL - 2 * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 2 : 1;
@@ -78,7 +84,17 @@ struct FwdCfg {
   static constexpr uint32_t FMT = DT == DT_BF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_S = idesc_make(128, 128, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_make(128, DV, FMT, FMT, 0, 1);
-  static constexpr int THREADS = 512;
+  static_assert(NG == 2 || NG == 4, "two or four activation groups");
+  // two groups come with a separate epilogue warpgroup; four fold the epilogue into the groups
+  static constexpr bool SEP_EPI = NG == 2;
+  static constexpr int THREADS = 128 + 128 * NG + (SEP_EPI ? 128 : 0);
+  static constexpr int ACT_WARP0 = 4, EPI_WARP0 = 4 + 4 * NG;
+  static constexpr int GCOLS = 128 / NG;            // score columns per activation group
+  static constexpr int OCOLS = DV / NG;             // O columns each group writes back
+  static_assert(OCOLS % 8 == 0, "value head dim must split into 8-column slices");
+  // O slice access width: 8 columns with four groups (96 registers a thread),
+  // else the widest that divides the slice and its column offset
+  static constexpr int OCH = NG == 4 ? 8 : (OCOLS % 32 == 0 ? 32 : (OCOLS % 16 == 0 ? 16 : 8));
   static constexpr uint32_t T_S = 0, T_P = 256, T_O = 384;  // TMEM column bases
 };
 
@@ -155,12 +171,12 @@ struct FwdSmem {
   uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, o_empty, pv_done[2];
-  uint64_t stat_full, stat_empty;
   uint32_t tmem_base;
   int abort_flag;
-  float red[2][2][128];  // softmax: per-group partial row max, by step parity
-  float stat_l[2][128];  // softmax: per-group partial row sums at item end
-  float stat_m[128];     // softmax: final running max at item end
+  float red[2][4][128];  // softmax: per-group partial row max, by step parity (NG <= 4)
+  float stat_l[4][128];  // softmax: per-group partial row sums at item end
+  float stat_m[128];     // softmax: final running max at item end (separate epilogue)
+  uint64_t stat_full, stat_empty;
 };
 
 // ---------------------------------------------------------------- activation groups
@@ -212,27 +228,46 @@ __device__ __forceinline__ void store_p_chunk(uint32_t taddr, const uint32_t (&r
   }
 }
 
-// P = where(c_lo <= col <= c_hi, act(scale * S), 0) for one group's 64
-// columns of an S tile; thread = one row (TMEM lane). t_s / t_p: this lane's
-// address of the group's first S / P column; col0 = 64 * group.
+// N-column (32, 16 or 8) TMEM loads and stores of one lane's registers.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 32) tmem_ld32(taddr, r);
+  else if constexpr (N == 16) tmem_ld16(taddr, r);
+  else tmem_ld8(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 32) {
+    tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(r));
+    tmem_st16(taddr + 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16));
+  } else if constexpr (N == 16) {
+    tmem_st16(taddr, r);
+  } else {
+    tmem_st8(taddr, r);
+  }
+}
+
+// P = where(c_lo <= col <= c_hi, act(scale * S), 0) for one group's GCOLS
+// columns of an S tile, 32 at a time; thread = one row (TMEM lane). t_s /
+// t_p: this lane's address of the group's first S / P column.
 template <class C, int ACT, bool MASKED>
-__device__ __forceinline__ bool act_half(uint32_t t_s, uint32_t t_p, int col0, const ActConsts& k, int c_lo,
-                                         int c_hi, const StepSync& sync) {
-  uint32_t sa[32], sb[32];
-  tmem_ld32(t_s, sa);
-  tmem_ld32(t_s + 32, sb);
-  tmem_ld_wait(sa);
-  tmem_ld_wait(sb);
+__device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0, const ActConsts& k, int c_lo,
+                                            int c_hi, const StepSync& sync) {
+  uint32_t sv[C::GCOLS / 32][32];
 #pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
-    uint32_t(&cur)[32] = ch ? sb : sa;
+  for (int ch = 0; ch < C::GCOLS / 32; ++ch) tmem_ld32(t_s + 32 * ch, sv[ch]);
+#pragma unroll
+  for (int ch = 0; ch < C::GCOLS / 32; ++ch) tmem_ld_wait(sv[ch]);
+#pragma unroll
+  for (int ch = 0; ch < C::GCOLS / 32; ++ch) {
+    const uint32_t(&sa)[32] = sv[ch];
     float p[32];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const f2_t r = act_pair<ACT>(f2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), k);
+      const f2_t r = act_pair<ACT>(f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1])), k);
       float v0 = f2_lo(r), v1 = f2_hi(r);
       if (MASKED) {
-        const int c = col0 + ch * 32 + 2 * e;
+        const int c = col0 + 32 * ch + 2 * e;
         v0 = (c >= c_lo && c <= c_hi) ? v0 : 0.0f;
         v1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? v1 : 0.0f;
       }
@@ -248,23 +283,26 @@ __device__ __forceinline__ bool act_half(uint32_t t_s, uint32_t t_p, int col0, c
 }
 
 template <class C, bool MASKED>
-__device__ __forceinline__ bool act_half_dispatch(int act, uint32_t t_s, uint32_t t_p, int col0, const ActConsts& k,
-                                                  int c_lo, int c_hi, const StepSync& sync) {
+__device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint32_t t_p, int col0,
+                                                     const ActConsts& k, int c_lo, int c_hi, const StepSync& sync) {
   switch (act) {
-    case ACT_IDENTITY: return act_half<C, ACT_IDENTITY, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_GELU: return act_half<C, ACT_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_GELU_TANH: return act_half<C, ACT_GELU_TANH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_FAST_GELU: return act_half<C, ACT_FAST_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_RELU: return act_half<C, ACT_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_RELU2: return act_half<C, ACT_RELU2, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_LEAKY_RELU: return act_half<C, ACT_LEAKY_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_SILU: return act_half<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    default: return act_half<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_IDENTITY: return act_quarter<C, ACT_IDENTITY, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_GELU: return act_quarter<C, ACT_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_GELU_TANH: return act_quarter<C, ACT_GELU_TANH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_FAST_GELU: return act_quarter<C, ACT_FAST_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_RELU: return act_quarter<C, ACT_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_RELU2: return act_quarter<C, ACT_RELU2, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_LEAKY_RELU: return act_quarter<C, ACT_LEAKY_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_SILU: return act_quarter<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    default: return act_quarter<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
   }
 }
 
-// Named barrier over the two activation groups (warps 4-11).
-__device__ __forceinline__ void act_groups_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barrier over the activation groups (warps 4 .. 4 + 4 NG - 1).
+template <int NG>
+__device__ __forceinline__ void act_groups_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(128 * NG) : "memory");
+}
 
 // ---------------------------------------------------------------- the kernel
 
@@ -293,7 +331,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], 256);
+      mbar_init(&sm.p_full[i], 128 * C::NG);
     }
     for (int i = 0; i < C::KST; ++i) {
       mbar_init(&sm.k_full[i], 1);
@@ -304,11 +342,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sm.v_empty[i], 1);
     }
     mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_empty, 128);
+    mbar_init(&sm.o_empty, C::SEP_EPI ? 128 : 128 * C::NG);
+    mbar_init(&sm.stat_full, 128 * C::NG);
+    mbar_init(&sm.stat_empty, 128);
     mbar_init(&sm.pv_done[0], 1);
     mbar_init(&sm.pv_done[1], 1);
-    mbar_init(&sm.stat_full, 256);
-    mbar_init(&sm.stat_empty, 128);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -447,24 +485,102 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         pc.advance(args, n_work);
       }
     }
-  } else if (warp >= 4 && warp < 12) {
-    // ------------------------------------------------ activation groups
-    const int grp = (warp - 4) / 4;
+  } else if (warp >= C::ACT_WARP0 && warp < C::ACT_WARP0 + 4 * C::NG) {
+    // ------------------------------------------------ activation groups (and epilogue when folded)
+    const int grp = (warp - C::ACT_WARP0) / 4;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    const int col0 = 64 * grp;
+    const int col0 = C::GCOLS * grp;
     float qk_scale = args.scale;
     if (C::DT == DT_E4M3 && args.descale != nullptr) qk_scale *= args.descale[0] * args.descale[1];
     const ActConsts act_k = make_act_consts(qk_scale);
     const float s_log2 = qk_scale * kLog2e;
-    uint32_t u = 0, stat_cnt = 0;
-    StepCursor c;
-    c.start(args, n_work);
-    bool ok = true;
-    while (c.active && ok) {
-      const FwdItem it = c.it;
+    float v_scale = 1.0f;
+    if (C::DT == DT_E4M3 && args.descale != nullptr) v_scale = args.descale[2];
+    using OutT = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
+    OutT* out = reinterpret_cast<OutT*>(args.out);
+    const bool gated = pv_gate_on_s(args.act);
+    uint32_t u = 0, o_cnt = 0, stat_cnt = 0;
+
+    // O of a finished item: this group's DV/4 columns of this thread's row.
+    // Run after the next item's first step so that the item's last PV has
+    // time to finish; the PV issuer waits o_empty before that item's first PV.
+    auto epilogue = [&](const FwdItem& it, float l, float m) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, o_cnt++ & 1, abort_flag))) return false;
+      tc_fence_after();
+      float f = v_scale, lse = 0.0f;
+      if (softmax) {  // row sum over the groups' partial sums
+        sm.stat_l[grp][row] = l;
+        act_groups_sync<C::NG>();
+        float lt = 0.0f;
+#pragma unroll
+        for (int g = 0; g < C::NG; ++g) lt += sm.stat_l[g][row];
+        f = lt > 0.0f ? v_scale / lt : 0.0f;
+        lse = lt > 0.0f ? m * 0.6931471805599453f + __logf(lt) : -INFINITY;
+      }
       const int qrow = it.r0 + row;
+      const bool row_valid = row < it.rows;
+      OutT* orow = out + (static_cast<size_t>(it.q_start + qrow) * pb.h_q + it.h) * C::DV + grp * C::OCOLS;
+      const uint32_t t_o = t_lane + C::T_O + grp * C::OCOLS;
+#pragma unroll
+      for (int c = 0; c < C::OCOLS; c += C::OCH) {
+        uint32_t o[C::OCH];
+        tmem_ld_cols(t_o + c, o);
+        tmem_ld_wait(o);
+        if (c + C::OCH == C::OCOLS) {
+          tc_fence_before();
+          mbar_arrive(&sm.o_empty);  // every TMEM read of O is done
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int q8 = 0; q8 < C::OCH / 8; ++q8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(o[8 * q8 + 2 * e]) * f, hi = __uint_as_float(o[8 * q8 + 2 * e + 1]) * f;
+              w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+            }
+            *reinterpret_cast<uint4*>(orow + c + 8 * q8) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      if (softmax && grp == 0 && row_valid && args.lse != nullptr)
+        args.lse[static_cast<size_t>(it.h) * pb.total_q + it.q_start + qrow] = lse;
+      return true;
+    };
+
+    // rescales this group's dv/NG columns of O by alpha (softmax)
+    auto rescale_o = [&](float alpha) {
+      const uint32_t t_o = t_lane + C::T_O + grp * C::OCOLS;
+#pragma unroll
+      for (int c = 0; c < C::OCOLS; c += C::OCH) {
+        uint32_t o[C::OCH];
+        tmem_ld_cols(t_o + c, o);
+        tmem_ld_wait(o);
+#pragma unroll
+        for (int e = 0; e < C::OCH; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st_cols(t_o + c, o);
+      }
+    };
+
+    bool ok = true, pend = false;
+    FwdItem pit{};
+    float pl = 0.0f, pm = 0.0f;
+    for (int round = 0; ok; ++round) {
+      const int pos = zigzag_pos(round, blockIdx.x, gridDim.x);
+      if (pos >= n_work) break;
+      const FwdItem it = fwd_decode(args, pos);
+      const int qrow = it.r0 + row;
+      if (it.n == 0) {  // no allowed key for any row: exact zeros
+        if (!C::SEP_EPI && row < it.rows) {
+          OutT* orow = out + (static_cast<size_t>(it.q_start + qrow) * pb.h_q + it.h) * C::DV + grp * C::OCOLS;
+          for (int q8 = 0; q8 < C::OCOLS / 8; ++q8) reinterpret_cast<uint4*>(orow)[q8] = make_uint4(0, 0, 0, 0);
+          if (softmax && grp == 0 && args.lse != nullptr)
+            args.lse[static_cast<size_t>(it.h) * pb.total_q + it.q_start + qrow] = -INFINITY;
+        }
+        continue;
+      }
       int kmin = 1, kmax = 0;
       if (!(row < it.rows && key_range(qrow, qrow, it.lq, it.lk, pb.causal, pb.window, kmin, kmax))) {
         kmin = 1;
@@ -478,76 +594,54 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         const int c_lo = kmin - j * kTileK, c_hi = kmax - j * kTileK;
         const uint32_t t_s = t_lane + C::T_S + b * 128 + col0;
-        const uint32_t t_p = t_lane + C::T_P + b * 64 + grp * (2 * C::P_COLS_PER_32);
-        const StepSync sync{&sm.pv_done[b], u, abort_flag, pv_gate_on_s(args.act)};
+        const uint32_t t_p = t_lane + C::T_P + b * 64 + grp * (C::GCOLS / 32) * C::P_COLS_PER_32;
+        const StepSync sync{&sm.pv_done[b], u, abort_flag, gated};
         if (!softmax) {
-          if (__all_sync(0xffffffffu, c_lo <= col0 && c_hi >= col0 + 63))
-            ok = act_half_dispatch<C, false>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
+          if (__all_sync(0xffffffffu, c_lo <= col0 && c_hi >= col0 + C::GCOLS - 1))
+            ok = act_quarter_dispatch<C, false>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
           else
-            ok = act_half_dispatch<C, true>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
+            ok = act_quarter_dispatch<C, true>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
           if (!ok) break;
         } else {
-          // online softmax in the log2 domain; both groups agree on the row max
-          uint32_t sa[32], sb[32];
-          tmem_ld32(t_s, sa);
-          tmem_ld32(t_s + 32, sb);
-          tmem_ld_wait(sa);
-          tmem_ld_wait(sb);
+          // online softmax in the log2 domain; the groups agree on the row max
+          uint32_t sa[C::GCOLS];
+          tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(sa));
+          if constexpr (C::GCOLS == 64) tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(sa + 32));
+          tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sa));
+          if constexpr (C::GCOLS == 64) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sa + 32));
           float mb = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c0 = col0 + e, c1 = col0 + 32 + e;
+          for (int e = 0; e < C::GCOLS; ++e) {
+            const int c0 = col0 + e;
             if (c0 >= c_lo && c0 <= c_hi) mb = fmaxf(mb, __uint_as_float(sa[e]) * s_log2);
-            if (c1 >= c_lo && c1 <= c_hi) mb = fmaxf(mb, __uint_as_float(sb[e]) * s_log2);
           }
           sm.red[u & 1][grp][row] = mb;
-          act_groups_sync();
-          mb = fmaxf(mb, sm.red[u & 1][grp ^ 1][row]);
+          act_groups_sync<C::NG>();
+#pragma unroll
+          for (int g = 0; g < C::NG; ++g) mb = fmaxf(mb, sm.red[u & 1][g][row]);
           // m is stale by at most 2^8: raise it (and rescale O) only past that
           const bool raise = mb > -INFINITY && (m == -INFINITY || mb > m + 8.0f);
           const float m_new = raise ? mb : m;
           const float alpha = raise && m != -INFINITY ? ex2_approx(m - m_new) : 1.0f;
           if (__any_sync(0xffffffffu, raise && m != -INFINITY) && j > it.lo) {
-            // O holds the previous step's PV: wait for it, then rescale this group's half of O
+            // O holds the previous step's PV: wait for it, then rescale this group's columns of O
             ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t t_o = t_lane + C::T_O + grp * (C::DV / 2);
-#pragma unroll 1
-            for (int cc = 0; cc + 32 <= C::DV / 2; cc += 32) {
-              uint32_t o[32];
-              tmem_ld32(t_o + cc, o);
-              tmem_ld_wait(o);
-              uint32_t w[16];
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(o[hf * 16 + e]) * alpha);
-                tmem_st16(t_o + cc + hf * 16, w);
-              }
-            }
-            if ((C::DV / 2) % 32 == 16) {
-              const uint32_t t16 = t_o + (C::DV / 2) - 16;
-              uint32_t o[16];
-              tmem_ld16(t16, o);
-              tmem_ld_wait(o);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st16(t16, o);
-            }
+            rescale_o(alpha);
           }
           l *= alpha;
           m = m_new;
           ok = sync.wait_p_buffer();
           if (!ok) break;
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            uint32_t(&cur)[32] = ch ? sb : sa;
+          for (int ch = 0; ch < C::GCOLS / 32; ++ch) {
             float p[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const int cc = col0 + ch * 32 + e;
-              const float v = (cc >= c_lo && cc <= c_hi) ? ex2_approx(__uint_as_float(cur[e]) * s_log2 - m) : 0.0f;
+              const int cc = col0 + 32 * ch + e;
+              const float v =
+                  (cc >= c_lo && cc <= c_hi) ? ex2_approx(__uint_as_float(sa[32 * ch + e]) * s_log2 - m) : 0.0f;
               l += v;
               p[e] = v;
             }
@@ -559,19 +653,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[b]);
+        if (!C::SEP_EPI && j == it.lo && pend) {
+          ok = epilogue(pit, pl, pm);
+          pend = false;
+          if (!ok) break;
+        }
       }
       if (!ok) break;
-      if (softmax) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.stat_empty, (stat_cnt++ & 1) ^ 1, abort_flag));
-        if (!ok) break;
-        sm.stat_l[grp][row] = l;
-        if (grp == 0) sm.stat_m[row] = m;
-        mbar_arrive(&sm.stat_full);
+      if constexpr (C::SEP_EPI) {
+        if (softmax) {  // hand the row statistics to the epilogue warps
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.stat_empty, (stat_cnt++ & 1) ^ 1, abort_flag));
+          if (!ok) break;
+          sm.stat_l[grp][row] = l;
+          if (grp == 0) sm.stat_m[row] = m;
+          mbar_arrive(&sm.stat_full);
+        }
+      } else {
+        pend = true;
+        pit = it;
+        pl = l;
+        pm = m;
       }
-      c.next_item(args, n_work);
     }
-  } else if (warp >= 12) {
-    // ------------------------------------------------ epilogue
+    if (ok && pend) ok = epilogue(pit, pl, pm);
+  } else if (C::SEP_EPI && warp >= C::EPI_WARP0) {
+    // ------------------------------------------------ epilogue warps (two activation groups)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t t_o = tbase + (static_cast<uint32_t>(quad * 32) << 16) + C::T_O;
@@ -604,7 +710,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (softmax) {
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.stat_full, stat_cnt++ & 1, abort_flag));
         if (!ok) break;
-        const float l = sm.stat_l[0][row] + sm.stat_l[1][row];
+        float l = 0.0f;
+#pragma unroll
+        for (int g = 0; g < C::NG; ++g) l += sm.stat_l[g][row];
         const float m = sm.stat_m[row];
         mbar_arrive(&sm.stat_empty);
         f = l > 0.0f ? v_scale / l : 0.0f;
@@ -651,15 +759,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 }
 
-template <int DQK, int DV, int DT>
-cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                           int grid, cudaStream_t stream) {
-  using C = FwdCfg<DQK, DV, DT>;
+// Four activation groups where the activation's arithmetic, not the tensor
+// core, sets the pace (16-bit GELU, tanh GELU, SiLU); two elsewhere, which
+// leaves each thread more registers.
+__host__ __device__ constexpr bool fwd_four_groups(int act, int dt) {
+  return dt != DT_E4M3 && (act == ACT_GELU || act == ACT_GELU_TANH || act == ACT_SILU);
+}
+
+template <int DQK, int DV, int DT, int NG>
+cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                          int grid, cudaStream_t stream) {
+  using C = FwdCfg<DQK, DV, DT, NG>;
   auto kern = gdpa_fwd_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
+}
+
+template <int DQK, int DV, int DT>
+cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                           int grid, cudaStream_t stream) {
+  if constexpr (DT != DT_E4M3) {
+    if (fwd_four_groups(a.act, DT)) return launch_fwd_ng<DQK, DV, DT, 4>(tq, tk, tv, a, grid, stream);
+  }
+  return launch_fwd_ng<DQK, DV, DT, 2>(tq, tk, tv, a, grid, stream);
 }
 
 }  // namespace gdpa

@@ -265,6 +265,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : GDPA_R8(0), GDPA_R8(8)
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];" : GDPA_R8(0) : "r"(taddr));
+}
 #undef GDPA_R8
 
 // Completes outstanding tcgen05.ld; the register operands tie the loaded
@@ -277,6 +280,9 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : GDPA_RW8(0), GDPA_RW8(8)::"memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : GDPA_RW8(0)::"memory");
 }
 #undef GDPA_RW8
 

@@ -65,8 +65,11 @@ def load_peaks():
 
 
 def kernel_sources_digest() -> str:
+    """Short hash of the CUDA kernel sources (ties recorded ncu counters to them)."""
     h = hashlib.sha1()
     for p in sorted(glob.glob(os.path.join(ROOT, "generalized_attention_recsys_gb300", "csrc", "*"))):
+        if not os.path.isfile(p) or not p.endswith((".cu", ".cuh", ".h")):
+            continue
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())

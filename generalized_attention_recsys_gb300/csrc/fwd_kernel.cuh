@@ -67,14 +67,25 @@ struct FwdCfg {
   static constexpr int V_BYTES = V_BOXES * BOX_BYTES;
   static constexpr int SMEM_LIMIT = 232448;  // 227 KB per block
   static constexpr int EXTRA_BYTES = 7168;   // barriers + softmax row exchange
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES;
+  static_assert(NG == 2 || NG == 4, "two or four activation groups");
+  // two groups come with a separate epilogue warpgroup; four fold the epilogue into the groups
+  static constexpr bool SEP_EPI = NG == 2;
+  // The separate epilogue stages O rows in shared memory (4 warps x 32 rows x
+  // 128 bytes) so that its global stores cover whole 128-byte segments; only
+  // where two K/V stages still fit beside it.
+  static constexpr int AVAIL_STAGED = SMEM_LIMIT - 1024 - EXTRA_BYTES - 16384;
+  static constexpr int QST_STAGED = (AVAIL_STAGED - 2 * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 2 : 1;
+  static constexpr int STAGE_BYTES =
+      SEP_EPI && (AVAIL_STAGED - QST_STAGED * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 16384 : 0;
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES - STAGE_BYTES;
   // Q double-buffered when two K/V stages still fit, else single
   static constexpr int QST = (AVAIL - 2 * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 2 : 1;
   static constexpr int FIT = (AVAIL - QST * Q_BYTES) / (K_BYTES + V_BYTES);
   static constexpr int KST = FIT > 4 ? 4 : FIT;
   static constexpr int VST = KST;
   static_assert(KST >= 2, "need at least two K/V stages");
-  static constexpr int SMEM_BYTES = 1024 + QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + EXTRA_BYTES;
+  static constexpr int SMEM_BYTES =
+      1024 + QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + STAGE_BYTES + EXTRA_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "tiles do not fit in shared memory");
   static constexpr int K_STEP = ESZ == 1 ? 32 : 16;  // K of one MMA instruction
   static_assert(DQK % K_STEP == 0, "head dim must be a multiple of the MMA K step");
@@ -84,9 +95,6 @@ struct FwdCfg {
   static constexpr uint32_t FMT = DT == DT_BF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_S = idesc_make(128, 128, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_make(128, DV, FMT, FMT, 0, 1);
-  static_assert(NG == 2 || NG == 4, "two or four activation groups");
-  // two groups come with a separate epilogue warpgroup; four fold the epilogue into the groups
-  static constexpr bool SEP_EPI = NG == 2;
   static constexpr int THREADS = 128 + 128 * NG + (SEP_EPI ? 128 : 0);
   static constexpr int ACT_WARP0 = 4, EPI_WARP0 = 4 + 4 * NG;
   static constexpr int GCOLS = 128 / NG;            // score columns per activation group
@@ -315,7 +323,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::QST * C::Q_BYTES;
   uint8_t* sV = sK + C::KST * C::K_BYTES;
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(sV + C::VST * C::V_BYTES);
+  uint8_t* sStage = sV + C::VST * C::V_BYTES;  // STAGE_BYTES (may be 0)
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(sStage + C::STAGE_BYTES);
   static_assert(sizeof(FwdSmem) <= C::EXTRA_BYTES, "barrier block too large");
 
   const int warp = threadIdx.x / 32;
@@ -718,25 +727,73 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         f = l > 0.0f ? v_scale / l : 0.0f;
         lse = l > 0.0f ? m * 0.6931471805599453f + __logf(l) : -INFINITY;
       }
+      // O from TMEM 32 columns at a time, packed to 16 bits; TMEM is released
+      // as soon as the last columns are in registers
+      constexpr int ECH = C::DV / 32;
+      if constexpr (C::STAGE_BYTES > 0) {
+        // through this warp's 32-row x 128-byte staging box (16-byte pieces
+        // XOR-swizzled by row), 64 columns at a time, so that eight lanes
+        // write one row's 128 contiguous bytes
+        uint8_t* stg = sStage + quad * 4096;
+        const size_t row_stride = static_cast<size_t>(pb.h_q) * C::DV;
+        OutT* obase = out + (static_cast<size_t>(it.q_start + it.r0 + quad * 32) * pb.h_q + it.h) * C::DV;
 #pragma unroll 1
-      for (int ch = 0; ch < C::DV / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(t_o + ch * 32, o);
-        tmem_ld_wait(o);
-        if (row_valid) {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float lo = __uint_as_float(o[2 * e]) * f, hi = __uint_as_float(o[2 * e + 1]) * f;
-            w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+        for (int ch = 0; ch < ECH; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(t_o + ch * 32, o);
+          tmem_ld_wait(o);
+          if (ch == ECH - 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.o_empty);  // every TMEM read of O is done
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(o[8 * q4 + 2 * e]) * f, hi = __uint_as_float(o[8 * q4 + 2 * e + 1]) * f;
+              w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+            }
+            const int piece = 4 * (ch & 1) + q4;
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if ((ch & 1) == 1 || ch == ECH - 1) {  // a 64-column half (or the last 32) is staged: write it out
+            __syncwarp();
+            const int piece = lane & 7, npieces = (ch & 1) ? 8 : 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + (lane >> 3);
+              if (quad * 32 + r < it.rows && piece < npieces) {
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((piece ^ (r & 7)) << 4));
+                *reinterpret_cast<uint4*>(obase + r * row_stride + (ch >> 1) * 64 + piece * 8) = v;
+              }
+            }
+            __syncwarp();
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < ECH; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(t_o + ch * 32, o);
+          tmem_ld_wait(o);
+          if (ch == ECH - 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.o_empty);
+          }
+          if (row_valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float lo = __uint_as_float(o[2 * e]) * f, hi = __uint_as_float(o[2 * e + 1]) * f;
+              w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sm.o_empty);
       if (softmax && row_valid && args.lse != nullptr) *lse_at = lse;
     }
   }

@@ -84,8 +84,12 @@ def test_zero_keys_give_zero_rows_and_empty_batch():
     assert out.numel() == 0
 
 
-def test_repeat_calls_are_bitwise_stable():
-    inp = inputs.custom(len(RAGGED), 2, 2, 128, 128, RAGGED, RAGGED, "gelu", seed=7)
-    a, _ = run_fwd(inp)
-    b, _ = run_fwd(inp)
+@pytest.mark.parametrize("act", ["gelu", "relu2", "softmax"])
+def test_repeat_calls_are_bitwise_stable(act):
+    # four activation groups (gelu) and two groups with the staged epilogue (relu2, softmax)
+    inp = inputs.custom(len(RAGGED), 2, 2, 128, 128, RAGGED, RAGGED, act, seed=7)
+    a, la = run_fwd(inp)
+    b, lb = run_fwd(inp)
     assert torch.equal(a, b)
+    if act == "softmax":
+        assert torch.equal(la, lb)

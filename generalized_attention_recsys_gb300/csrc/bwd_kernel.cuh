@@ -310,6 +310,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  // registers: control warpgroup 96, elementwise warpgroups 168, drain warpgroup 80
+  // (128 * 96 + 256 * 168 + 128 * 80 = 65536 = 512 * 128 launched)
+  static_assert(C::NG == 2 && C::THREADS == 512, "register split assumes two elementwise warpgroups");
+  static_assert(128 * 96 + 256 * 168 + 128 * 80 <= C::THREADS * 128, "register split exceeds the launch");
+
+  if (warp < C::ACT_WARP0) regs_dec<96>();  // each role sets its warpgroup's budget first
 
   if (warp == 0 || warp == 2 || warp == 3) {
     // ------------------------------------------------ TMA producers
@@ -460,6 +466,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   } else if (warp >= C::ACT_WARP0 && warp < C::DRAIN_WARP0) {
     // ------------------------------------------------ elementwise groups + dK/dV epilogue
+    regs_inc<168>();
     const int w = (warp - C::ACT_WARP0) / 4;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // key row within the block
@@ -547,6 +554,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   } else if (warp >= C::DRAIN_WARP0) {
     // ------------------------------------------------ dQ drain: TMEM -> smem -> TMA reduce-add
+    regs_dec<80>();
     // Each warp owns 32 query rows (its TMEM lane quadrant). Per 32-column
     // chunk it stages a 32 x 32 fp32 box in shared memory (128-byte swizzle)
     // and lane 0 adds it into the fp32 accumulator with one bulk tensor

@@ -130,6 +130,18 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 // Wait until all of this thread's bulk groups have completed (writes done).
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Per-warpgroup register budgets (all 128 threads of the warpgroup execute
+// it). The sum over warpgroups must stay within the registers the block was
+// launched with, or an increase waits forever.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- tcgen05: TMEM management
 
 // Whole warp: allocate ncols (power of two >= 32) TMEM columns; the base

@@ -638,6 +638,9 @@ cudaError_t launch_bwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            cudaStream_t stream) {
   using C = BwdCfg<DQK, DV, DT>;
   auto kern = gdpa_bwd_kernel<C>;
+  // the per-role register split assumes 128 registers a thread at launch
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < 128) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);

@@ -112,7 +112,8 @@ def make_shape(q, k, v, batch: int) -> GdpaShape:
                      DTYPES[q.dtype])
 
 
-def gdpa_workspace_bytes(shape: GdpaShape, max_seqlen_q: int, max_seqlen_k: int, is_bwd: bool) -> int:
+def gdpa_workspace_bytes(shape: GdpaShape, max_seqlen_q: int, max_seqlen_k: int, is_bwd: int) -> int:
+    """is_bwd: 0 forward, 1 backward, 2 deterministic backward (C-ABI gdpa_workspace_bytes)."""
     return int(load().gdpa_workspace_bytes(ctypes.byref(shape), max_seqlen_q, max_seqlen_k, int(is_bwd)))
 
 
@@ -161,7 +162,7 @@ def gdpa_bwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    nb = gdpa_workspace_bytes(shape, max_seqlen_q, max_seqlen_k, True)
+    nb = gdpa_workspace_bytes(shape, max_seqlen_q, max_seqlen_k, 2 if deterministic else 1)
     ws = _workspace(nb, q.device, workspace)
     st = lib.gdpa_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                       int(max_seqlen_q), int(max_seqlen_k), _act(act), float(scale), int(bool(causal)),

@@ -121,6 +121,12 @@ size_t bwd_list_cap(const gdpa_shape* s) {
 }
 size_t list_bytes(size_t cap) { return round256(16 + 8 * cap); }
 
+// Deterministic backward: one fp32 dQ slice [total_q, h_q, d_qk] per key block.
+size_t dq_part_bytes(const gdpa_shape* s, int max_k) {
+  const size_t nkv = max_k > 0 ? (static_cast<size_t>(max_k) + kTileK - 1) / kTileK : 0;
+  return nkv * static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float);
+}
+
 int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int window) {
   (void)causal;
   (void)window;
@@ -234,6 +240,7 @@ size_t gdpa_workspace_bytes(const gdpa_shape* s, int max_q, int max_k, int is_bw
   size_t b = list_bytes(bwd_list_cap(s));
   b += round256(static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float));  // dQ accumulator
   b += round256(static_cast<size_t>(s->total_q) * s->h_q * sizeof(float));            // softmax rowsum(dO*O)
+  if (is_bwd == 2) b += round256(dq_part_bytes(s, max_k));                          // deterministic dQ slices
   return b;
 }
 
@@ -298,7 +305,6 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   if (st != GDPA_OK) return st;
   if (s->dtype == GDPA_E4M3) return GDPA_ERR_UNSUPPORTED;
   if (s->d_qk > 128) return GDPA_ERR_UNSUPPORTED;  // (192,128) backward: TMEM plan holds dims <= 128
-  if (deterministic) return GDPA_ERR_UNSUPPORTED;
   if (s->batch == 0 || (s->total_q == 0 && s->total_k == 0)) return GDPA_OK;
   if ((cu_q == nullptr) != (cu_k == nullptr)) return GDPA_ERR_INVALID;
   if (!cu_q && (s->total_q != s->batch * max_q || s->total_k != s->batch * max_k)) return GDPA_ERR_INVALID;
@@ -309,7 +315,8 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   for (const void* p : need_k)
     if (s->total_k > 0 && (!p || !aligned16(p))) return GDPA_ERR_INVALID;
   if (act == GDPA_ACT_SOFTMAX && (!out || !lse || !aligned16(out))) return GDPA_ERR_INVALID;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, 1))
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, deterministic ? 2 : 1))
     return GDPA_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const int nsm = sm_count();
@@ -324,6 +331,8 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   float* dq_acc = reinterpret_cast<float*>(ws);
   ws += round256(static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float));
   float* drow = reinterpret_cast<float*>(ws);
+  ws += round256(static_cast<size_t>(s->total_q) * s->h_q * sizeof(float));
+  float* dq_part = deterministic ? reinterpret_cast<float*>(ws) : nullptr;
 
   build_worklist<<<1, 1024, 0, stream>>>(pb, 1, wl, cap);
   if (cudaGetLastError() != cudaSuccess) return GDPA_ERR_CUDA;
@@ -341,6 +350,7 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.dk = dk;
   a.dv = dv;
   a.dq_acc = dq_acc;
+  a.dq_part = dq_part;
   a.drow = drow;
   a.d_qk = s->d_qk;
   a.d_v = s->d_v;

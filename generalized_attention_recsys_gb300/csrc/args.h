@@ -32,6 +32,8 @@ struct BwdArgs {
   void* dk;          // [total_k, h_kv, dqk]
   void* dv;          // [total_k, h_kv, dv]
   float* dq_acc;     // workspace: fp32 [total_q, h_q, dqk]
+  float* dq_part;    // deterministic mode: fp32 [ceil(max_k / 128), total_q, h_q, dqk], one slice per
+                     // key block; NULL otherwise
   float* drow;       // workspace: softmax rowsum(dO * O), [h_q, total_q]
   int d_qk, d_v, dtype;
 };

@@ -1,5 +1,6 @@
 // Backward launcher: clears the fp32 dQ accumulator (and, for softmax,
-// computes rowsum(dO * O)), runs the main kernel, then converts dQ.
+// computes rowsum(dO * O)), runs the main kernel, then converts dQ; in
+// deterministic mode it adds the per-key-block dQ slices in a fixed order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -21,6 +22,12 @@ namespace {
 
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 
 // Zero the dQ accumulator; softmax: drow[h, t] = sum_d dO[t, h, d] * O[t, h, d].
 template <typename T>
@@ -66,6 +73,51 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
+// Deterministic mode: dQ of each (token, head) row is the sum, in key-block
+// order, of the slices written by the key blocks whose backward work item
+// covered the row's 128-row query block (the same query_range test the work
+// items use, so only written slices are read). One warp per row.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Problem pb, int d, T* dq) {
+  const int lane = threadIdx.x & 31;
+  const size_t nwarps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
+  const size_t rows = static_cast<size_t>(pb.total_q) * pb.h_q;
+  for (size_t r = blockIdx.x * static_cast<size_t>(blockDim.x / 32) + threadIdx.x / 32; r < rows; r += nwarps) {
+    const int t = static_cast<int>(r / pb.h_q);
+    int b;  // the sequence holding token t
+    if (pb.cu_q == nullptr) {
+      b = t / pb.max_q;
+    } else {
+      int lo = 0, hi = pb.batch - 1;  // last b with cu_q[b] <= t
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (pb.cu_q[mid] <= t) lo = mid;
+        else hi = mid - 1;
+      }
+      b = lo;
+    }
+    int qs, lq, ks, lk;
+    seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
+    seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
+    const int qb = (t - qs) / kTileQ;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // columns lane, lane + 32, ... (d <= 128)
+    const int nkv = lk > 0 ? (lk + kTileK - 1) / kTileK : 0;
+    for (int j = 0; j < nkv; ++j) {
+      const int k0 = j * kTileK, k1 = min(k0 + kTileK, lk) - 1;
+      int rmin, rmax;
+      if (!query_range(k0, k1, lq, lk, pb.causal, pb.window, rmin, rmax)) continue;
+      if (qb < rmin / kTileQ || qb > rmax / kTileQ) continue;
+      const float* src = part + (static_cast<size_t>(j) * pb.total_q * pb.h_q + r) * d;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        if (lane + 32 * m < d) acc[m] += src[lane + 32 * m];
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (lane + 32 * m < d) dq[r * d + lane + 32 * m] = from_f<T>(acc[m]);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T* dq) {
   const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
@@ -78,7 +130,8 @@ __global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T*
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdq, const BwdArgs& a, int grid, cudaStream_t stream, cudaEvent_t before,
                        cudaEvent_t after) {
-  const size_t n4 = static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4;
+  const bool ordered = a.dq_part != nullptr;  // deterministic mode: no accumulator to clear
+  const size_t n4 = ordered ? 0 : static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4;
   const int eg = grid * 8;  // elementwise kernels: 8 blocks of 256 per SM
   float* drow = a.act == 9 ? a.drow : nullptr;
   if (a.dtype == DT_FP16)
@@ -100,6 +153,14 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   }
   if (e != cudaSuccess) return e;
   if (after) cudaEventRecord(after, stream);
+  if (ordered) {
+    if (a.dtype == DT_FP16)
+      bwd_post_ordered<__half><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk, static_cast<__half*>(a.dq));
+    else
+      bwd_post_ordered<__nv_bfloat16><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk,
+                                                             static_cast<__nv_bfloat16*>(a.dq));
+    return cudaGetLastError();
+  }
   if (a.dtype == DT_FP16)
     bwd_post<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4,
                                              static_cast<__half*>(a.dq));

@@ -583,6 +583,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           mbar_arrive(&sm.dq_empty);
           continue;
         }
+        if (args.dq_part != nullptr) {
+          // deterministic mode: this key block's dQ tile goes to its own slice; a
+          // later kernel adds the slices in key-block order
+          float* dst = args.dq_part + ((static_cast<size_t>(it.k0 / kTileK) * pb.total_q + it.q_start + q0 + row) *
+                                           pb.h_q + h) * C::DQK;
+#pragma unroll 1
+          for (int ch = 0; ch < C::DQK / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(t_dq + ch * 32, o);
+            tmem_ld_wait(o);
+            if (ch == C::DQK / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(&sm.dq_empty);
+            }
+            if (valid) {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                reinterpret_cast<uint4*>(dst + ch * 32)[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+            }
+          }
+          continue;
+        }
         // every staged chunk commits one bulk group, so the ring's box parity
         // and the group count stay in step
 #pragma unroll 1

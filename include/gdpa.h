@@ -98,9 +98,11 @@ typedef struct gdpa_shape {
   int dtype;   /* gdpa_dtype */
 } gdpa_shape;
 
-/* Bytes of device workspace that gdpa_fwd (is_bwd = 0) or gdpa_bwd
- * (is_bwd = 1) needs for this problem; 0 for an invalid shape. The size
- * depends only on the arguments given here. */
+/* Bytes of device workspace that gdpa_fwd (is_bwd = 0), gdpa_bwd
+ * (is_bwd = 1) or gdpa_bwd with deterministic != 0 (is_bwd = 2) needs for
+ * this problem; 0 for an invalid shape. The size depends only on the
+ * arguments given here. The deterministic backward adds one fp32 dQ slice
+ * [total_q, h_q, d_qk] per 128-key block of the longest key sequence. */
 size_t gdpa_workspace_bytes(const gdpa_shape* shape, int max_seqlen_q, int max_seqlen_k, int is_bwd);
 
 /* Forward. scale multiplies Q K^T before the activation (1/sqrt(d_qk) is the
@@ -121,10 +123,15 @@ int gdpa_fwd(const gdpa_shape* shape, const void* q, const void* k, const void* 
 /* Backward (bf16/fp16 only). Arguments as for gdpa_fwd; out and lse are read
  * only for GDPA_ACT_SOFTMAX (they must be the forward's results) and may be
  * NULL otherwise. dout has out's layout; dq, dk, dv have q's, k's and v's.
- * dq is accumulated in fp32 inside the workspace and converted at the end;
- * dk/dv of a kv head sum the contributions of its query-head group.
- * deterministic != 0 is reserved for an ordered dQ reduction; the current
- * build accepts only 0 and returns GDPA_ERR_UNSUPPORTED otherwise. */
+ * dk/dv of a kv head sum the contributions of its query-head group in a
+ * fixed order, so they are the same bits on every call. dq sums the
+ * contributions of all key blocks: with deterministic = 0 they are added
+ * into an fp32 accumulator in the workspace in whatever order the key
+ * blocks finish (results may differ in the last bits between calls); with
+ * deterministic != 0 each key block writes its own fp32 slice and a final
+ * kernel adds the slices in key-block order, so dq is bitwise reproducible
+ * (at the cost of the slices' memory, see gdpa_workspace_bytes, and their
+ * HBM traffic). FA's flash_attn_varlen_func(deterministic=...) is the model. */
 int gdpa_bwd(const gdpa_shape* shape, const void* q, const void* k, const void* v,
              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
              int max_seqlen_k, int act, float scale, int causal, int window, const void* out,

@@ -56,6 +56,10 @@ def test_workspace_bytes(lib):
     # backward holds an fp32 dQ accumulator
     assert bwd >= 256 * 4 * 128 * 4
     assert _lib.gdpa_workspace_bytes(_shape(h_q=3), 128, 128, False) == 0
+    # the deterministic backward adds one fp32 dQ slice per 128-key block of max_seqlen_k
+    for max_k, nkv in ((128, 1), (129, 2), (300, 3)):
+        det = _lib.gdpa_workspace_bytes(s, 128, max_k, 2)
+        assert det - _lib.gdpa_workspace_bytes(s, 128, max_k, 1) == nkv * 256 * 4 * 128 * 4
 
 
 @pytest.mark.parametrize("kw,status", [

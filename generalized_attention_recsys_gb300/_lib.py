@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libgdpa.so")
 NOALLOC_SCRATCH_BYTES = 512 * 1024
 DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 ACTS = {"identity": 0, "gelu": 1, "gelu_tanh": 2, "fast_gelu": 3, "relu": 4, "relu2": 5,
-        "leaky_relu": 6, "silu": 7, "hardswish": 8, "softmax": 9}
+        "leaky_relu": 6, "silu": 7, "hardswish": 8, "softmax": 9, "fast_gelu_bf16": 10, "fast_silu": 11}
 EXPORTS = ("gdpa_workspace_bytes", "gdpa_fwd", "gdpa_bwd", "gdpa_get_status", "gdpa_error_string",
            "gdpa_set_profile_events", "gdpa_fwd_noalloc", "gdpa_num_sms")
 

@@ -134,7 +134,7 @@ int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int
   if (s->batch < 0 || s->total_q < 0 || s->total_k < 0 || max_q < 0 || max_k < 0) return GDPA_ERR_INVALID;
   if (s->h_q <= 0 || s->h_kv <= 0 || s->h_q % s->h_kv != 0) return GDPA_ERR_INVALID;
   if (s->dtype < GDPA_BF16 || s->dtype > GDPA_E4M3) return GDPA_ERR_INVALID;
-  if (act < GDPA_ACT_IDENTITY || act > GDPA_ACT_SOFTMAX) return GDPA_ERR_INVALID;
+  if (act < GDPA_ACT_IDENTITY || act > GDPA_ACT_FAST_SILU) return GDPA_ERR_INVALID;
   const bool ok_dims = (s->d_qk == 64 && s->d_v == 64) || (s->d_qk == 96 && s->d_v == 96) ||
                        (s->d_qk == 128 && s->d_v == 128) || (s->d_qk == 192 && s->d_v == 128);
   if (!ok_dims) return GDPA_ERR_UNSUPPORTED;

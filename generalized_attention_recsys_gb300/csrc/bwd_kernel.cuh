@@ -247,6 +247,8 @@ __device__ __forceinline__ void bwd_pass1_dispatch(int act, uint32_t t_lane, int
     GDPA_BWD_CASE(ACT_LEAKY_RELU)
     GDPA_BWD_CASE(ACT_SILU)
     GDPA_BWD_CASE(ACT_HARDSWISH)
+    GDPA_BWD_CASE(ACT_FAST_GELU_BF16)
+    GDPA_BWD_CASE(ACT_FAST_SILU)
     default: bwd_pass1<C, ACT_SOFTMAX, MASKED>(t_lane, w, k, c_lo, c_hi, lse, col_base, col_max);
   }
 #undef GDPA_BWD_CASE

@@ -269,6 +269,19 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
 #pragma unroll
   for (int ch = 0; ch < C::GCOLS / 32; ++ch) {
     const uint32_t(&sa)[32] = sv[ch];
+    uint32_t pk[16];
+    if constexpr (ACT == ACT_FAST_GELU_BF16 && C::DT == DT_BF16) {
+      // already bf16 pairs: store them as they come, masking by halves
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        uint32_t w = fast_gelu_bf16_pair(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1]), k);
+        if (MASKED) {
+          const int c = col0 + 32 * ch + 2 * e;
+          w &= ((c >= c_lo && c <= c_hi) ? 0x0000FFFFu : 0u) | ((c + 1 >= c_lo && c + 1 <= c_hi) ? 0xFFFF0000u : 0u);
+        }
+        pk[e] = w;
+      }
+    } else {
     float p[32];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -282,8 +295,8 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
       p[2 * e] = v0;
       p[2 * e + 1] = v1;
     }
-    uint32_t pk[16];
     pack_p_chunk<C::DT>(p, pk);
+    }
     if (ch == 0 && !sync.wait_p_buffer()) return false;  // first store into the buffer
     store_p_chunk<C::DT>(t_p + ch * C::P_COLS_PER_32, pk);
   }
@@ -302,6 +315,8 @@ __device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint
     case ACT_RELU2: return act_quarter<C, ACT_RELU2, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
     case ACT_LEAKY_RELU: return act_quarter<C, ACT_LEAKY_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
     case ACT_SILU: return act_quarter<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_FAST_GELU_BF16: return act_quarter<C, ACT_FAST_GELU_BF16, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    case ACT_FAST_SILU: return act_quarter<C, ACT_FAST_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
     default: return act_quarter<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
   }
 }

@@ -84,7 +84,9 @@ typedef enum gdpa_act {
   GDPA_ACT_LEAKY_RELU = 6,
   GDPA_ACT_SILU = 7,
   GDPA_ACT_HARDSWISH = 8,
-  GDPA_ACT_SOFTMAX = 9
+  GDPA_ACT_SOFTMAX = 9,
+  GDPA_ACT_FAST_GELU_BF16 = 10, /* FastGELU (BF16): the tanh form evaluated in packed bf16 */
+  GDPA_ACT_FAST_SILU = 11       /* FastSiLU: z (1 + tanh(z / 2)) / 2 with the hardware tanh */
 } gdpa_act;
 
 typedef struct gdpa_shape {

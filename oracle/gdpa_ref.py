@@ -40,6 +40,10 @@ design notes):
 * ``fast_gelu`` is the same function as ``gelu_tanh`` (the page lists it as a
   faster evaluation, not a different function) -- parity unpinned by the
   pages;
+* ``fast_gelu_bf16`` ("FastGELU (BF16)") is again ``gelu_tanh``, evaluated by
+  the kernels in bf16 arithmetic, and ``fast_silu`` ("FastSiLU") is ``silu``
+  evaluated through tanh; the oracle computes the exact functions -- parity
+  unpinned by the pages;
 * LeakyReLU slope 0.01 -- parity unpinned by the pages;
 * derivatives at kinks follow PyTorch's conventions;
 * causal with Lq != Lk is bottom-right aligned: allowed iff j <= i + Lk - Lq;
@@ -67,6 +71,8 @@ ACTIVATIONS = (
     "silu",
     "hardswish",
     "softmax",
+    "fast_gelu_bf16",
+    "fast_silu",
 )
 
 LEAKY_SLOPE = 0.01
@@ -86,7 +92,7 @@ def act_fwd(name: str, z: torch.Tensor) -> torch.Tensor:
         return z.clone()
     if name == "gelu":
         return 0.5 * z * (1.0 + torch.erf(z * _INV_SQRT_2))
-    if name in ("gelu_tanh", "fast_gelu"):
+    if name in ("gelu_tanh", "fast_gelu", "fast_gelu_bf16"):
         u = _SQRT_2_OVER_PI * (z + _TANH_CUBIC * z * z * z)
         return 0.5 * z * (1.0 + torch.tanh(u))
     if name == "relu":
@@ -96,7 +102,7 @@ def act_fwd(name: str, z: torch.Tensor) -> torch.Tensor:
         return r * r
     if name == "leaky_relu":
         return torch.where(z > 0, z, LEAKY_SLOPE * z)
-    if name == "silu":
+    if name in ("silu", "fast_silu"):
         return z / (1.0 + torch.exp(-z))
     if name == "hardswish":
         return z * torch.clamp(z + 3.0, 0.0, 6.0) / 6.0
@@ -113,7 +119,7 @@ def act_grad(name: str, z: torch.Tensor) -> torch.Tensor:
         cdf = 0.5 * (1.0 + torch.erf(z * _INV_SQRT_2))
         pdf = _INV_SQRT_2PI * torch.exp(-0.5 * z * z)
         return cdf + z * pdf
-    if name in ("gelu_tanh", "fast_gelu"):
+    if name in ("gelu_tanh", "fast_gelu", "fast_gelu_bf16"):
         u = _SQRT_2_OVER_PI * (z + _TANH_CUBIC * z * z * z)
         t = torch.tanh(u)
         du = _SQRT_2_OVER_PI * (1.0 + 3.0 * _TANH_CUBIC * z * z)
@@ -124,7 +130,7 @@ def act_grad(name: str, z: torch.Tensor) -> torch.Tensor:
         return torch.where(z > 0, 2.0 * z, zero)
     if name == "leaky_relu":
         return torch.where(z > 0, one, LEAKY_SLOPE * one)
-    if name == "silu":
+    if name in ("silu", "fast_silu"):
         sig = 1.0 / (1.0 + torch.exp(-z))
         return sig * (1.0 + z * (1.0 - sig))
     if name == "hardswish":

@@ -19,9 +19,14 @@ from gpu_util import ensure_built
 
 pytestmark = pytest.mark.gpu
 
-ELEMENTWISE = ["identity", "gelu", "gelu_tanh", "fast_gelu", "relu", "relu2", "leaky_relu", "silu", "hardswish"]
-# approximation bound of the device forward evaluation, as a multiple of max(1, |z|)
-FWD_BOUND = {"gelu": 2e-5, "fast_gelu": 6e-4, "gelu_tanh": 2e-5, "silu": 2e-5}
+ELEMENTWISE = ["identity", "gelu", "gelu_tanh", "fast_gelu", "relu", "relu2", "leaky_relu", "silu", "hardswish",
+               "fast_gelu_bf16", "fast_silu"]
+# approximation bound of the device forward evaluation, as a multiple of max(1, |z|).
+# fast_gelu_bf16 rounds s^2, the cubic, u, z/2, tanh(u) and the result to bf16:
+# emulating that (tanh exact, then rounded) gives at most 1.8e-3 beyond the one
+# bf16 ulp allowed below; 6e-3 leaves room for the hardware bf16 tanh.
+FWD_BOUND = {"gelu": 2e-5, "fast_gelu": 6e-4, "gelu_tanh": 2e-5, "silu": 2e-5, "fast_gelu_bf16": 6e-3,
+             "fast_silu": 6e-4}
 
 
 def _grid(lo, hi, n):

@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 RAGGED = [1, 127, 128, 129, 300, 0, 513, 64]
 ALL_ACTS = ["identity", "gelu", "gelu_tanh", "fast_gelu", "relu", "relu2", "leaky_relu", "silu",
-            "hardswish", "softmax"]
+            "hardswish", "softmax", "fast_gelu_bf16", "fast_silu"]
 
 
 def test_tiny_fixed_length():

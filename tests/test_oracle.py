@@ -64,6 +64,8 @@ _LIB = {
     "leaky_relu": lambda z: F.leaky_relu(z, LEAKY_SLOPE),
     "silu": F.silu,
     "hardswish": F.hardswish,
+    "fast_gelu_bf16": lambda z: F.gelu(z, approximate="tanh"),
+    "fast_silu": F.silu,
 }
 
 

@@ -557,17 +557,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   } else if (warp >= C::DRAIN_WARP0) {
     // ------------------------------------------------ dQ drain: TMEM -> smem -> TMA reduce-add
     regs_dec<80>();
-    // Each warp owns 32 query rows (its TMEM lane quadrant). Per 32-column
-    // chunk it stages a 32 x 32 fp32 box in shared memory (128-byte swizzle)
-    // and lane 0 adds it into the fp32 accumulator with one bulk tensor
-    // reduce; a ring of two boxes per warp lets the next chunk's TMEM read
-    // overlap the previous reduce. Rows past the sequence end are staged as
-    // zeros, so adding them into the next sequence's rows changes nothing.
+    // Each warp owns 32 query rows (its TMEM lane quadrant). A 32-column chunk
+    // of those rows is staged as a 32 x 32 fp32 box in shared memory
+    // (128-byte swizzle) and lane 0 adds it into the fp32 accumulator with
+    // one bulk tensor reduce; each warp has two boxes, so chunks move in
+    // pairs. Rows past the sequence end are staged as zeros, so adding them
+    // into the next sequence's rows changes nothing.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // query row within the tile
     const uint32_t t_dq = tbase + (static_cast<uint32_t>(quad * 32) << 16) + C::T_DQ;
-    uint8_t* stage = sDQ + quad * 2 * C::DQ_CHUNK_BYTES;
-    uint32_t dq_cnt = 0, chunk_it = 0;
+    uint8_t* stage_base = sDQ + quad * 2 * C::DQ_CHUNK_BYTES;  // this warp's two 32 x 32 fp32 boxes
+    constexpr int NCH = C::DQK / 32, NPAIR = (NCH + 1) / 2;
+    uint32_t dq_cnt = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int pos = zigzag_pos(round, blockIdx.x, G);
@@ -607,33 +608,51 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           continue;
         }
-        // every staged chunk commits one bulk group, so the ring's box parity
-        // and the group count stay in step
-#pragma unroll 1
-        for (int ch = 0; ch < C::DQK / 32; ++ch, ++chunk_it) {
-          uint32_t o[32];
-          tmem_ld32(t_dq + ch * 32, o);
-          if (ch == C::DQK / 32 - 1) {
-            tmem_ld_wait(o);
-            tc_fence_before();
-            mbar_arrive(&sm.dq_empty);  // every TMEM read of this tile is done
-          }
-          uint8_t* box = stage + (chunk_it & 1) * C::DQ_CHUNK_BYTES;
-          if (lane == 0) bulk_wait_group_read<1>();  // the reduce that last read this box is done with it
-          __syncwarp();
-          tmem_ld_wait(o);
+        // Chunks go through registers two at a time (one staging box each).
+        // The TMEM columns are released as soon as the last pair is in
+        // registers; every reduce issue and every wait for a box to be read
+        // comes after that, off the path of the next dP^T GEMM.
+        auto stage = [&](int bi, const uint32_t(&o)[32]) {
+          uint8_t* box = stage_base + bi * C::DQ_CHUNK_BYTES;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = valid ? make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]) : make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
           }
+        };
+        auto reduce_pair = [&](int c0) {  // lane 0: add boxes 0 (and 1) into chunks c0 (and c0 + 1), one bulk group
+          tma_reduce_add_3d(&tm_dq, stage_base, c0 * 32, h, it.q_start + q0 + quad * 32);
+          if (c0 + 1 < NCH) tma_reduce_add_3d(&tm_dq, stage_base + C::DQ_CHUNK_BYTES, (c0 + 1) * 32, h,
+                                              it.q_start + q0 + quad * 32);
+          bulk_commit_group();
+        };
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's reduces are done reading both boxes
+        __syncwarp();
+#pragma unroll
+        for (int pr = 0; pr < NPAIR; ++pr) {
+          const int c0 = 2 * pr;
+          uint32_t a[32], b[32];
+          tmem_ld32(t_dq + c0 * 32, a);
+          if (c0 + 1 < NCH) tmem_ld32(t_dq + (c0 + 1) * 32, b);
+          tmem_ld_wait(a);
+          if (c0 + 1 < NCH) tmem_ld_wait(b);
+          if (pr == NPAIR - 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.dq_empty);  // every TMEM read of this tile is done
+          }
+          if (pr > 0) {  // add the previous pair, then wait until its boxes have been read
+            if (lane == 0) {
+              reduce_pair(c0 - 2);
+              bulk_wait_group_read<0>();
+            }
+            __syncwarp();
+          }
+          stage(0, a);
+          if (c0 + 1 < NCH) stage(1, b);
           fence_async_shared();
           __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d(&tm_dq, box, ch * 32, h, it.q_start + q0 + quad * 32);
-            bulk_commit_group();
-          }
         }
+        if (lane == 0) reduce_pair(2 * (NPAIR - 1));
       }
     }
     if (lane == 0) bulk_wait_group_all();

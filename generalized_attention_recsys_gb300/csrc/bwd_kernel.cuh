@@ -161,17 +161,24 @@ __device__ __forceinline__ void bwd_pass1(uint32_t t_lane, int w, const BwdConst
     uint32_t pk[16], gk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      const f2_t sv = f2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1]));
-      f2_t pv, gv;
+      float p0, p1, g0, g1;
       if constexpr (ACT == ACT_SOFTMAX) {
+        const f2_t sv = f2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1]));
         const int i0 = min(col_base + col0 + e, col_max), i1 = min(col_base + col0 + e + 1, col_max);
         const f2_t a = fma2(sv, f2(k.scale * kLog2e), f2(-__ldg(lse + i0) * kLog2e, -__ldg(lse + i1) * kLog2e));
-        pv = f2(ex2_approx(f2_lo(a)), ex2_approx(f2_hi(a)));
-        gv = pv;
+        p0 = g0 = ex2_approx(f2_lo(a));
+        p1 = g1 = ex2_approx(f2_hi(a));
+      } else if constexpr (act_scalar_grad_form(ACT)) {
+        hardswish_grad(__uint_as_float(cur[e]), k, p0, g0);
+        hardswish_grad(__uint_as_float(cur[e + 1]), k, p1, g1);
       } else {
-        act_pair_grad<ACT>(sv, k, pv, gv);
+        f2_t pv, gv;
+        act_pair_grad<ACT>(f2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])), k, pv, gv);
+        p0 = f2_lo(pv);
+        p1 = f2_hi(pv);
+        g0 = f2_lo(gv);
+        g1 = f2_hi(gv);
       }
-      float p0 = f2_lo(pv), p1 = f2_hi(pv), g0 = f2_lo(gv), g1 = f2_hi(gv);
       if (MASKED) {
         const bool ok0 = (col0 + e) >= c_lo && (col0 + e) <= c_hi;
         const bool ok1 = (col0 + e + 1) >= c_lo && (col0 + e + 1) <= c_hi;

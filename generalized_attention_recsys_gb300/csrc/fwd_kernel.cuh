@@ -54,9 +54,13 @@
 
 namespace gdpa {
 
-template <int DQK_, int DV_, int DT_, int NG_>
+// SOFTMAX_: the online-softmax kernel (GDPA_ACT_SOFTMAX); the elementwise
+// activations get kernels of their own, so neither carries the other's code.
+template <int DQK_, int DV_, int DT_, int NG_, bool SOFTMAX_ = false>
 struct FwdCfg {
   static constexpr int DQK = DQK_, DV = DV_, DT = DT_, NG = NG_;
+  static constexpr bool SOFTMAX = SOFTMAX_;
+  static_assert(!SOFTMAX || NG == 2, "softmax runs with two activation groups");
   static constexpr int ESZ = DT == DT_E4M3 ? 1 : 2;
   static constexpr int BOX_ELEMS = 128 / ESZ;  // elements per 128-byte swizzle row
   static constexpr int BOX_BYTES = 128 * 128;  // one 128-row x 128-byte swizzled box
@@ -303,22 +307,43 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
   return true;
 }
 
+// Each kernel configuration compiles only the activations the launcher can
+// start it with (four groups: 16-bit GELU, tanh GELU and SiLU; two groups:
+// the rest, or every activation for e4m3), so branches it never takes cost
+// it no registers.
 template <class C, bool MASKED>
 __device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint32_t t_p, int col0,
                                                      const ActConsts& k, int c_lo, int c_hi, const StepSync& sync) {
-  switch (act) {
-    case ACT_IDENTITY: return act_quarter<C, ACT_IDENTITY, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_GELU: return act_quarter<C, ACT_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_GELU_TANH: return act_quarter<C, ACT_GELU_TANH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_FAST_GELU: return act_quarter<C, ACT_FAST_GELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_RELU: return act_quarter<C, ACT_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_RELU2: return act_quarter<C, ACT_RELU2, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_LEAKY_RELU: return act_quarter<C, ACT_LEAKY_RELU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_SILU: return act_quarter<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_FAST_GELU_BF16: return act_quarter<C, ACT_FAST_GELU_BF16, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    case ACT_FAST_SILU: return act_quarter<C, ACT_FAST_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-    default: return act_quarter<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+#define GDPA_ACT_CASE(A) \
+  case A: return act_quarter<C, A, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+  if constexpr (C::NG == 4) {
+    switch (act) {
+      GDPA_ACT_CASE(ACT_GELU)
+      GDPA_ACT_CASE(ACT_GELU_TANH)
+      default: return act_quarter<C, ACT_SILU, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
+    }
+  } else {
+    switch (act) {
+      GDPA_ACT_CASE(ACT_IDENTITY)
+      GDPA_ACT_CASE(ACT_FAST_GELU)
+      GDPA_ACT_CASE(ACT_RELU)
+      GDPA_ACT_CASE(ACT_RELU2)
+      GDPA_ACT_CASE(ACT_LEAKY_RELU)
+      GDPA_ACT_CASE(ACT_FAST_GELU_BF16)
+      GDPA_ACT_CASE(ACT_FAST_SILU)
+      default: break;
+    }
+    if constexpr (C::DT == DT_E4M3) {
+      switch (act) {
+        GDPA_ACT_CASE(ACT_GELU)
+        GDPA_ACT_CASE(ACT_GELU_TANH)
+        GDPA_ACT_CASE(ACT_SILU)
+        default: break;
+      }
+    }
+    return act_quarter<C, ACT_HARDSWISH, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
   }
+#undef GDPA_ACT_CASE
 }
 
 // Named barrier over the activation groups (warps 4 .. 4 + 4 NG - 1).
@@ -347,7 +372,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const Problem& pb = args.pb;
   const int n_work = args.work->count * pb.h_q;
   volatile int* abort_flag = &sm.abort_flag;
-  const bool softmax = args.act == ACT_SOFTMAX;
+  constexpr bool softmax = C::SOFTMAX;
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
@@ -620,7 +645,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t t_s = t_lane + C::T_S + b * 128 + col0;
         const uint32_t t_p = t_lane + C::T_P + b * 64 + grp * (C::GCOLS / 32) * C::P_COLS_PER_32;
         const StepSync sync{&sm.pv_done[b], u, abort_flag, gated};
-        if (!softmax) {
+        if constexpr (!softmax) {
           if (__all_sync(0xffffffffu, c_lo <= col0 && c_hi >= col0 + C::GCOLS - 1))
             ok = act_quarter_dispatch<C, false>(args.act, t_s, t_p, col0, act_k, c_lo, c_hi, sync);
           else
@@ -838,10 +863,10 @@ __host__ __device__ constexpr bool fwd_four_groups(int act, int dt) {
   return dt != DT_E4M3 && (act == ACT_GELU || act == ACT_GELU_TANH || act == ACT_SILU);
 }
 
-template <int DQK, int DV, int DT, int NG>
+template <int DQK, int DV, int DT, int NG, bool SOFTMAX = false>
 cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                           int grid, cudaStream_t stream) {
-  using C = FwdCfg<DQK, DV, DT, NG>;
+  using C = FwdCfg<DQK, DV, DT, NG, SOFTMAX>;
   auto kern = gdpa_fwd_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -855,6 +880,7 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if constexpr (DT != DT_E4M3) {
     if (fwd_four_groups(a.act, DT)) return launch_fwd_ng<DQK, DV, DT, 4>(tq, tk, tv, a, grid, stream);
   }
+  if (a.act == ACT_SOFTMAX) return launch_fwd_ng<DQK, DV, DT, 2, true>(tq, tk, tv, a, grid, stream);
   return launch_fwd_ng<DQK, DV, DT, 2>(tq, tk, tv, a, grid, stream);
 }
 

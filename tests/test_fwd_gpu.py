@@ -63,6 +63,31 @@ def test_fp16(act):
     assert_close(out, ref, FWD_TOL, "out fp16")
 
 
+@pytest.mark.parametrize("act", ALL_ACTS)
+def test_every_activation_fp16(act):
+    # every fp16 kernel configuration: four activation groups (GELU, tanh GELU, SiLU), two groups
+    # (the other elementwise activations) and the softmax kernel, each compiled for its own set
+    inp = inputs.custom(len(RAGGED), 2, 1, 128, 128, RAGGED, RAGGED, act, dtype="fp16", seed=6, with_dout=False)
+    out, lse = run_fwd(inp)
+    assert out.dtype == torch.float16
+    ref, ref_lse = ref_fwd(inp)
+    assert_close(out, ref, FWD_TOL, f"out fp16 [{act}]")
+    if act == "softmax":
+        fin = torch.isfinite(ref_lse)
+        assert (lse.cpu().double()[fin] - ref_lse[fin]).abs().max() < 1e-3
+
+
+@pytest.mark.parametrize("act", ALL_ACTS)
+def test_every_activation_fp8(act):
+    # e4m3 runs every activation with two groups: the elementwise kernel and the softmax kernel
+    lens = [200, 129, 1, 450, 0, 300]
+    inp = inputs.custom(len(lens), 2, 2, 128, 128, lens, lens, act, dtype="e4m3", seed=7, with_dout=False)
+    out, _ = run_fwd(inp)
+    assert out.dtype == torch.bfloat16
+    ref, _ = ref_fwd(inp)
+    assert_close(out, ref, FP8_TOL, f"out e4m3 [{act}]")
+
+
 @pytest.mark.parametrize("dims,h_kv,causal,window", [((128, 128), 4, False, -1), ((192, 128), 1, True, 100),
                                                     ((64, 64), 2, True, -1)])
 def test_fp8(dims, h_kv, causal, window):

@@ -329,10 +329,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
-  // registers: control warpgroup 96, elementwise warpgroups 168, drain warpgroup 80
-  // (128 * 96 + 256 * 168 + 128 * 80 = 65536 = 512 * 128 launched)
+  // registers: control warpgroup 96, elementwise warpgroups 160, drain warpgroup 96
+  // (128 * 96 + 256 * 160 + 128 * 96 = 65536 = 512 * 128 launched)
   static_assert(C::NG == 2 && C::THREADS == 512, "register split assumes two elementwise warpgroups");
-  static_assert(128 * 96 + 256 * 168 + 128 * 80 <= C::THREADS * 128, "register split exceeds the launch");
+  static_assert(128 * 96 + 256 * 160 + 128 * 96 <= C::THREADS * 128, "register split exceeds the launch");
 
   if (warp < C::ACT_WARP0) regs_dec<96>();  // each role sets its warpgroup's budget first
 
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   } else if (warp >= C::ACT_WARP0 && warp < C::DRAIN_WARP0) {
     // ------------------------------------------------ elementwise groups + dK/dV epilogue
-    regs_inc<168>();
+    regs_inc<160>();
     const int w = (warp - C::ACT_WARP0) / 4;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // key row within the block
@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   } else if (warp >= C::DRAIN_WARP0) {
     // ------------------------------------------------ dQ drain: TMEM -> smem -> TMA reduce-add
-    regs_dec<80>();
+    regs_dec<96>();
     // Each warp owns 32 query rows (its TMEM lane quadrant). A 32-column chunk
     // of those rows is staged as a 32 x 32 fp32 box in shared memory
     // (128-byte swizzle) and lane 0 adds it into the fp32 accumulator with

@@ -79,8 +79,12 @@ def test_host_validation_rejects_before_launch(lib, kw, status):
 
 def test_bad_activation_and_fp8_backward(lib):
     s = _shape()
-    assert lib.gdpa_fwd(ctypes.byref(s), None, None, None, None, None, 128, 128, 42, 0.1, 0, -1,
-                        None, None, None, None, 0, None) == _lib.GDPA_ERR_INVALID
+    assert max(_lib.ACTS.values()) == 11 and sorted(_lib.ACTS.values()) == list(range(12))
+    for bad in (-1, 12, 42):  # just outside the enum on both sides, and far outside
+        assert lib.gdpa_fwd(ctypes.byref(s), None, None, None, None, None, 128, 128, bad, 0.1, 0, -1,
+                            None, None, None, None, 0, None) == _lib.GDPA_ERR_INVALID
+        assert lib.gdpa_bwd(ctypes.byref(s), None, None, None, None, None, 128, 128, bad, 0.1, 0, -1,
+                            None, None, None, None, None, None, 0, None, 0, None) == _lib.GDPA_ERR_INVALID
     s8 = _shape(dtype=2)
     assert lib.gdpa_bwd(ctypes.byref(s8), None, None, None, None, None, 128, 128, 1, 0.1, 0, -1,
                         None, None, None, None, None, None, 0, None, 0, None) == _lib.GDPA_ERR_UNSUPPORTED

@@ -10,8 +10,19 @@
 #include <mutex>
 
 #include "../../include/gdpa.h"
+#include "act.cuh"
 #include "args.h"
 #include "common.cuh"
+
+// The kernels' activation codes are the C ABI's, value for value.
+static_assert(gdpa::ACT_IDENTITY == GDPA_ACT_IDENTITY && gdpa::ACT_GELU == GDPA_ACT_GELU &&
+                  gdpa::ACT_GELU_TANH == GDPA_ACT_GELU_TANH && gdpa::ACT_FAST_GELU == GDPA_ACT_FAST_GELU &&
+                  gdpa::ACT_RELU == GDPA_ACT_RELU && gdpa::ACT_RELU2 == GDPA_ACT_RELU2 &&
+                  gdpa::ACT_LEAKY_RELU == GDPA_ACT_LEAKY_RELU && gdpa::ACT_SILU == GDPA_ACT_SILU &&
+                  gdpa::ACT_HARDSWISH == GDPA_ACT_HARDSWISH && gdpa::ACT_SOFTMAX == GDPA_ACT_SOFTMAX &&
+                  gdpa::ACT_FAST_GELU_BF16 == GDPA_ACT_FAST_GELU_BF16 && gdpa::ACT_FAST_SILU == GDPA_ACT_FAST_SILU &&
+                  gdpa::ACT_COUNT == GDPA_ACT_FAST_SILU + 1,
+              "activation codes differ between the kernels and gdpa.h");
 
 namespace gdpa {
 

@@ -26,20 +26,6 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
-
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " elect.sync _|p, 0xffffffff;\n"
-      " selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -255,48 +241,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Predicated forms for an issuing warp whose lanes all run the issue loop
-// (its operands then stay warp-uniform); only the lane with `issue` != 0
-// executes the instruction. A commit tracks the MMAs of the lane that
-// executes it, so the same lane must issue both.
-__device__ __forceinline__ void mma_f16_ss_p(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate, uint32_t issue) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p, q;\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " setp.ne.b32 q, %5, 0;\n"
-      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
-      : "memory");
-}
-__device__ __forceinline__ void mma_f16_ts_p(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate, uint32_t issue) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p, q;\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " setp.ne.b32 q, %5, 0;\n"
-      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit_p(uint64_t* bar, uint32_t issue) {
-  asm volatile(
-      "{\n"
-      " .reg .pred q;\n"
-      " setp.ne.b32 q, %1, 0;\n"
-      " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
-      "}\n" ::"r"(smem_u32(bar)),
-      "r"(issue)
-      : "memory");
-}
-// A shared-memory descriptor moved by `bytes` (the start-address field holds
-// address / 16 in 14 bits; shared-memory addresses stay below 2^18, so the
-// addition cannot carry out of the field).
-__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 // ---------------------------------------------------------------- tcgen05: TMEM <-> registers
 // 32x32b shape: thread t of warp w reads lane 32*(w%4)+t, consecutive columns.

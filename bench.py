@@ -34,6 +34,13 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# More hardware work queues than CUDA's default 8, so that the end-to-end
+# leg's two copy streams (host->device, device->host) and the compute stream
+# are less likely to share one queue and serialise behind each other. Read at
+# CUDA initialisation, so it has to be set before torch touches the GPU; a
+# value already in the environment wins.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 import torch  # noqa: E402
 
 METRIC = "GDPA fwd & bwd TFLOP/s (useful, jagged) and % of GB300 dense tensor-core peak"

@@ -73,7 +73,11 @@ typedef enum gdpa_dtype { GDPA_BF16 = 0, GDPA_FP16 = 1, GDPA_E4M3 = 2 } gdpa_dty
 
 /* Activations ("Features" on the gdpa/README.md page). GELU_TANH is
  * GELUApprox; FAST_GELU evaluates the same tanh-form GELU; LEAKY_RELU uses
- * slope 0.01; derivatives at kinks follow PyTorch. */
+ * slope 0.01; derivatives at kinks follow PyTorch. FAST_GELU_BF16 and
+ * FAST_SILU are cheaper forward evaluations of GELU_TANH and SILU (results
+ * within about 6e-3 * max(1, |z|) beyond one bf16 ulp, and 6e-4 * max(1, |z|),
+ * of the exact functions); their backward uses the GELU_TANH and SILU
+ * derivatives. */
 typedef enum gdpa_act {
   GDPA_ACT_IDENTITY = 0,
   GDPA_ACT_GELU = 1,

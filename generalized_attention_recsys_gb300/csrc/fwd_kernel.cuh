@@ -11,9 +11,10 @@
 // same flattened stream of steps across items. Warp roles (128 + 128 NG
 // threads, NG = 2 or 4 activation groups):
 //   warp 0       TMA producer: Q tiles (one item ahead, double-buffered) and
-//                a K/V ring
-//   warp 1       MMA issuer for S = Q K^T (one thread)
-//   warp 2       MMA issuer for O += P V (one thread)
+//                the K ring
+//   warp 1       MMA issuer for S = Q K^T (whole warp; one elected lane issues)
+//   warp 2       MMA issuer for O += P V (likewise)
+//   warp 3       TMA producer: the V ring
 //   warps 4..    NG activation groups of four warps (one per TMEM lane
 //                quadrant); group g owns score columns [g 128/NG, +128/NG)
 //                of every S tile and, at the end of an item, O columns
@@ -56,6 +57,11 @@ namespace gdpa {
 
 // SOFTMAX_: the online-softmax kernel (GDPA_ACT_SOFTMAX); the elementwise
 // activations get kernels of their own, so neither carries the other's code.
+// Largest n <= cap with n * per <= avail.
+__host__ __device__ constexpr int fwd_ring_stages(int avail, int per, int cap) {
+  return avail / per > cap ? cap : avail / per;
+}
+
 template <int DQK_, int DV_, int DT_, int NG_, bool SOFTMAX_ = false>
 struct FwdCfg {
   static constexpr int DQK = DQK_, DV = DV_, DT = DT_, NG = NG_;
@@ -70,24 +76,25 @@ struct FwdCfg {
   static constexpr int K_BYTES = QK_BOXES * BOX_BYTES;
   static constexpr int V_BYTES = V_BOXES * BOX_BYTES;
   static constexpr int SMEM_LIMIT = 232448;  // 227 KB per block
-  static constexpr int EXTRA_BYTES = 7168;   // barriers + softmax row exchange
+  // barriers (and, for softmax, the row statistics exchange)
+  static constexpr int EXTRA_BYTES = SOFTMAX ? 8192 : 1024;
   static_assert(NG == 2 || NG == 4, "two or four activation groups");
   // two groups come with a separate epilogue warpgroup; four fold the epilogue into the groups
   static constexpr bool SEP_EPI = NG == 2;
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES;
+  // Q double-buffered when two K and two V stages still fit, else single
+  static constexpr int QST = AVAIL - 2 * Q_BYTES >= 2 * (K_BYTES + V_BYTES) ? 2 : 1;
+  // K needs the deeper ring: S(u) must wait for K(u), whose load can start
+  // only once S(u - KST) has released its stage, while V(u) is wanted one
+  // GEMM later. Then V takes what is left (at most as many stages as K).
+  static constexpr int KST = fwd_ring_stages(AVAIL - QST * Q_BYTES - 2 * V_BYTES, K_BYTES, 4);
+  static constexpr int VST = fwd_ring_stages(AVAIL - QST * Q_BYTES - KST * K_BYTES, V_BYTES, KST);
+  static_assert(KST >= 2 && VST >= 2, "need at least two K and two V stages");
   // The separate epilogue stages O rows in shared memory (4 warps x 32 rows x
-  // 128 bytes) so that its global stores cover whole 128-byte segments; only
-  // where two K/V stages still fit beside it.
-  static constexpr int AVAIL_STAGED = SMEM_LIMIT - 1024 - EXTRA_BYTES - 16384;
-  static constexpr int QST_STAGED = (AVAIL_STAGED - 2 * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 2 : 1;
+  // 128 bytes) so that its global stores cover whole 128-byte segments,
+  // where that still fits beside the rings.
   static constexpr int STAGE_BYTES =
-      SEP_EPI && (AVAIL_STAGED - QST_STAGED * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 16384 : 0;
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES - STAGE_BYTES;
-  // Q double-buffered when two K/V stages still fit, else single
-  static constexpr int QST = (AVAIL - 2 * Q_BYTES) / (K_BYTES + V_BYTES) >= 2 ? 2 : 1;
-  static constexpr int FIT = (AVAIL - QST * Q_BYTES) / (K_BYTES + V_BYTES);
-  static constexpr int KST = FIT > 4 ? 4 : FIT;
-  static constexpr int VST = KST;
-  static_assert(KST >= 2, "need at least two K/V stages");
+      SEP_EPI && QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + 16384 <= AVAIL ? 16384 : 0;
   static constexpr int SMEM_BYTES =
       1024 + QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + STAGE_BYTES + EXTRA_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "tiles do not fit in shared memory");
@@ -183,12 +190,16 @@ struct FwdSmem {
   uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, o_empty, pv_done[2];
+  uint64_t stat_full, stat_empty;
   uint32_t tmem_base;
   int abort_flag;
-  float red[2][4][128];  // softmax: per-group partial row max, by step parity (NG <= 4)
-  float stat_l[4][128];  // softmax: per-group partial row sums at item end
-  float stat_m[128];     // softmax: final running max at item end (separate epilogue)
-  uint64_t stat_full, stat_empty;
+};
+
+// Softmax only: the row statistics the activation groups exchange.
+struct FwdSoftmaxSmem {
+  float red[2][4][128];  // per-group partial row max, by step parity (NG <= 4)
+  float stat_l[4][128];  // per-group partial row sums at item end
+  float stat_m[128];     // final running max at item end (separate epilogue)
 };
 
 // ---------------------------------------------------------------- activation groups
@@ -285,11 +296,26 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
         }
         pk[e] = w;
       }
+    } else if constexpr (ACT == ACT_GELU && C::DT == DT_BF16) {
+      // mixed tanh form / polynomial, packed by truncation (constants carry the bias)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        uint32_t w =
+            pack_trunc_bf16x2(gelu_mixed_pair<true>(e, f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1])), k));
+        if (MASKED) {
+          const int c = col0 + 32 * ch + 2 * e;
+          w &= ((c >= c_lo && c <= c_hi) ? 0x0000FFFFu : 0u) | ((c + 1 >= c_lo && c + 1 <= c_hi) ? 0xFFFF0000u : 0u);
+        }
+        pk[e] = w;
+      }
     } else {
     float p[32];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const f2_t r = act_pair<ACT>(f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1])), k);
+      const f2_t sp = f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1]));
+      f2_t r;
+      if constexpr (ACT == ACT_GELU) r = gelu_mixed_pair<false>(e, sp, k);
+      else r = act_pair<ACT>(sp, k);
       float v0 = f2_lo(r), v1 = f2_hi(r);
       if (MASKED) {
         const int c = col0 + 32 * ch + 2 * e;
@@ -365,7 +391,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* sV = sK + C::KST * C::K_BYTES;
   uint8_t* sStage = sV + C::VST * C::V_BYTES;  // STAGE_BYTES (may be 0)
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(sStage + C::STAGE_BYTES);
-  static_assert(sizeof(FwdSmem) <= C::EXTRA_BYTES, "barrier block too large");
+  static_assert(sizeof(FwdSmem) <= 1024, "barrier block too large");
+  static_assert(!C::SOFTMAX || 1024 + sizeof(FwdSoftmaxSmem) <= C::EXTRA_BYTES, "softmax block too large");
+  // only softmax configurations reserve room for it
+  FwdSoftmaxSmem& ssm = *reinterpret_cast<FwdSoftmaxSmem*>(reinterpret_cast<uint8_t*>(&sm) + 1024);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -405,38 +434,45 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
   }
+  if (warp == 3 && lane == 0) prefetch_tmap(&tm_v);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: Q tiles and the K ring
     if (lane == 0) {
-      uint32_t k_it = 0, v_it = 0;
+      uint32_t k_it = 0;
       StepCursor kc, qc;
       kc.start(args, n_work);
       qc.start(args, n_work);
       bool ok = true;
-      auto load_q = [&]() {  // Q tile of the item under qc, then move qc on
+      // Q tile of the item under qc into its slot, then move qc on. With
+      // block = false it loads only if the slot is already free, so that a
+      // Q slot still in use does not hold back the K ring.
+      auto load_q = [&](bool block) {
         const int slot = qc.item_idx % C::QST;
-        ok = mbar_wait(&sm.q_empty[slot], ((qc.item_idx / C::QST) & 1) ^ 1, abort_flag);
-        if (!ok) return;
+        const uint32_t par = ((qc.item_idx / C::QST) & 1) ^ 1;
+        if (block) {
+          ok = mbar_wait(&sm.q_empty[slot], par, abort_flag);
+          if (!ok) return;
+        } else if (!mbar_test_wait(&sm.q_empty[slot], par)) {
+          return;
+        }
         mbar_arrive_expect_tx(&sm.q_full[slot], C::Q_BYTES);
         for (int bx = 0; bx < C::QK_BOXES; ++bx)
           tma_load_3d(sQ + slot * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[slot], bx * C::BOX_ELEMS,
                       qc.it.h, qc.it.q_start + qc.it.r0);
         qc.next_item(args, n_work);
       };
-      if (qc.active) load_q();
       while (kc.active && ok) {
-        // double-buffered Q: when an item starts, fetch the next item's Q
-        if (C::QST == 2 && kc.j == kc.it.lo && qc.active) {
-          load_q();
-          if (!ok) break;
-        }
+        // the Q of the item whose K comes next is on its way first
+        while (ok && qc.active && qc.item_idx <= kc.item_idx) load_q(true);
+        if (!ok) break;
+        // the following item's Q as soon as its slot frees
+        if (qc.active && qc.item_idx == kc.item_idx + 1) load_q(false);
         const int ks = k_it % C::KST;
         ok = mbar_wait(&sm.k_empty[ks], ((k_it / C::KST) & 1) ^ 1, abort_flag);
         if (!ok) break;
@@ -445,24 +481,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           tma_load_3d(sK + ks * C::K_BYTES + bx * C::BOX_BYTES, &tm_k, &sm.k_full[ks], bx * C::BOX_ELEMS, kc.it.g,
                       kc.it.k_start + kc.j * kTileK);
         ++k_it;
+        kc.advance(args, n_work);
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------ TMA producer: the V ring
+    // (its own thread, so that a V stage still in use by PV does not hold
+    // back the K loads, which S needs a GEMM earlier)
+    if (lane == 0) {
+      uint32_t v_it = 0;
+      StepCursor vc;
+      vc.start(args, n_work);
+      bool ok = true;
+      while (vc.active && ok) {
         const int vs = v_it % C::VST;
         ok = mbar_wait(&sm.v_empty[vs], ((v_it / C::VST) & 1) ^ 1, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.v_full[vs], C::V_BYTES);
         for (int bx = 0; bx < C::V_BOXES; ++bx)
-          tma_load_3d(sV + vs * C::V_BYTES + bx * C::BOX_BYTES, &tm_v, &sm.v_full[vs], bx * C::BOX_ELEMS, kc.it.g,
-                      kc.it.k_start + kc.j * kTileK);
+          tma_load_3d(sV + vs * C::V_BYTES + bx * C::BOX_BYTES, &tm_v, &sm.v_full[vs], bx * C::BOX_ELEMS, vc.it.g,
+                      vc.it.k_start + vc.j * kTileK);
         ++v_it;
-        const int prev_idx = kc.item_idx;
-        kc.advance(args, n_work);
-        // single Q buffer: the next item's Q follows its predecessor's last S
-        if (C::QST == 1 && kc.active && kc.item_idx != prev_idx && qc.active) load_q();
+        vc.advance(args, n_work);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer: S = Q K^T
-    if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK);
+    // ------------------------------------------------ MMA issuer: S = Q K^T (whole warp, one lane issues)
+    {
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024), dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       uint32_t k_it = 0, u = 0;
       const bool gate = pv_gate_on_s(args.act);
       StepCursor sc;
@@ -479,30 +525,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (ok && sc.j == sc.it.lo) ok = mbar_wait(&sm.q_full[slot], (sc.item_idx / C::QST) & 1, abort_flag);
         const int ks = k_it % C::KST;
         if (ok) ok = mbar_wait(&sm.k_full[ks], (k_it / C::KST) & 1, abort_flag);
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        const uint32_t a0 = sQa + slot * C::Q_BYTES, b0 = sKa + ks * C::K_BYTES;
+        const uint64_t a0 = sdesc_at(dq0, slot * C::Q_BYTES), b0 = sdesc_at(dk0, ks * C::K_BYTES);
         const uint32_t d = tbase + C::T_S + b * 128;
 #pragma unroll
         for (int k = 0; k < C::S_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
           if constexpr (C::DT == DT_E4M3)
-            mma_f8_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::IDESC_S, k > 0);
+            mma_f8_ss_w(d, sdesc_at(a0, off), sdesc_at(b0, off), C::IDESC_S, k > 0);
           else
-            mma_f16_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::IDESC_S, k > 0);
+            mma_f16_ss_w(d, sdesc_at(a0, off), sdesc_at(b0, off), C::IDESC_S, k > 0);
         }
-        mma_commit(&sm.s_full[b]);
-        mma_commit(&sm.k_empty[ks]);
+        mma_commit_w(&sm.s_full[b]);
+        mma_commit_w(&sm.k_empty[ks]);
         ++k_it;
-        if (sc.j == sc.it.hi) mma_commit(&sm.q_empty[slot]);
+        if (sc.j == sc.it.hi) mma_commit_w(&sm.q_empty[slot]);
         ++u;
         sc.advance(args, n_work);
       }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------ MMA issuer: O += P V
-    if (lane == 0) {
-      const uint32_t sVa = smem_u32(sV);
+    // ------------------------------------------------ MMA issuer: O += P V (whole warp, one lane issues)
+    {
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sV), C::BOX_BYTES, 1024);
       uint32_t v_it = 0, u = 0, o_cnt = 0;
       StepCursor pc;
       pc.start(args, n_work);
@@ -513,23 +559,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (ok && pc.j == pc.it.lo) ok = mbar_wait(&sm.o_empty, (o_cnt++ & 1) ^ 1, abort_flag);
         const int vs = v_it % C::VST;
         if (ok) ok = mbar_wait(&sm.v_full[vs], (v_it / C::VST) & 1, abort_flag);
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        const uint32_t b0 = sVa + vs * C::V_BYTES;
+        const uint64_t b0 = sdesc_at(dv0, vs * C::V_BYTES);
         const bool acc = pc.j > pc.it.lo;
 #pragma unroll
         for (int k = 0; k < C::PV_MMAS; ++k) {
           const uint32_t a_t = tbase + C::T_P + b * 64 + k * (C::K_STEP * C::ESZ / 4);
-          const uint64_t bd = sdesc_sw128(b0 + k * C::K_STEP * 128, C::BOX_BYTES, 1024);
+          const uint64_t bd = sdesc_at(b0, k * C::K_STEP * 128);
           if constexpr (C::DT == DT_E4M3)
-            mma_f8_ts(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
+            mma_f8_ts_w(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
           else
-            mma_f16_ts(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
+            mma_f16_ts_w(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
         }
-        mma_commit(&sm.v_empty[vs]);
-        mma_commit(&sm.pv_done[b]);
+        mma_commit_w(&sm.v_empty[vs]);
+        mma_commit_w(&sm.pv_done[b]);
         ++v_it;
-        if (pc.j == pc.it.hi) mma_commit(&sm.o_full);
+        if (pc.j == pc.it.hi) mma_commit_w(&sm.o_full);
         ++u;
         pc.advance(args, n_work);
       }
@@ -543,12 +589,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int col0 = C::GCOLS * grp;
     float qk_scale = args.scale;
     if (C::DT == DT_E4M3 && args.descale != nullptr) qk_scale *= args.descale[0] * args.descale[1];
-    const ActConsts act_k = make_act_consts(qk_scale);
+    const ActConsts act_k = make_act_consts(qk_scale, C::DT == DT_BF16 ? kTruncBias : 1.0f);
     const float s_log2 = qk_scale * kLog2e;
     float v_scale = 1.0f;
     if (C::DT == DT_E4M3 && args.descale != nullptr) v_scale = args.descale[2];
     using OutT = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
     OutT* out = reinterpret_cast<OutT*>(args.out);
+    // 32-byte stores need a 32-byte aligned output (rows of dv = 128 are)
+    const bool out_v8 = (reinterpret_cast<uintptr_t>(args.out) & 31) == 0;
     const bool gated = pv_gate_on_s(args.act);
     uint32_t u = 0, o_cnt = 0, stat_cnt = 0;
 
@@ -560,11 +608,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tc_fence_after();
       float f = v_scale, lse = 0.0f;
       if (softmax) {  // row sum over the groups' partial sums
-        sm.stat_l[grp][row] = l;
+        ssm.stat_l[grp][row] = l;
         act_groups_sync<C::NG>();
         float lt = 0.0f;
 #pragma unroll
-        for (int g = 0; g < C::NG; ++g) lt += sm.stat_l[g][row];
+        for (int g = 0; g < C::NG; ++g) lt += ssm.stat_l[g][row];
         f = lt > 0.0f ? v_scale / lt : 0.0f;
         lse = lt > 0.0f ? m * 0.6931471805599453f + __logf(lt) : -INFINITY;
       }
@@ -572,25 +620,45 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const bool row_valid = row < it.rows;
       OutT* orow = out + (static_cast<size_t>(it.q_start + qrow) * pb.h_q + it.h) * C::DV + grp * C::OCOLS;
       const uint32_t t_o = t_lane + C::T_O + grp * C::OCOLS;
+      // every TMEM load first, so that O is released to the next item's PV
+      // before the conversion and the global stores
+      uint32_t o[C::OCOLS / C::OCH][C::OCH];
 #pragma unroll
-      for (int c = 0; c < C::OCOLS; c += C::OCH) {
-        uint32_t o[C::OCH];
-        tmem_ld_cols(t_o + c, o);
-        tmem_ld_wait(o);
-        if (c + C::OCH == C::OCOLS) {
-          tc_fence_before();
-          mbar_arrive(&sm.o_empty);  // every TMEM read of O is done
+      for (int c = 0; c < C::OCOLS / C::OCH; ++c) tmem_ld_cols(t_o + c * C::OCH, o[c]);
+#pragma unroll
+      for (int c = 0; c < C::OCOLS / C::OCH; ++c) tmem_ld_wait(o[c]);
+      tc_fence_before();
+      mbar_arrive(&sm.o_empty);  // every TMEM read of O is done
+      if constexpr (C::OCOLS == 32) {
+        // 64 bytes of the row: paired 32-byte stores where the output allows
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float lo = __uint_as_float(o[e / 4][(2 * e) % 8]) * f;
+          const float hi = __uint_as_float(o[e / 4][(2 * e) % 8 + 1]) * f;
+          w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
         }
-        if (row_valid) {
+        if (out_v8) {
+          store_rows64_paired(reinterpret_cast<uint8_t*>(orow), static_cast<size_t>(pb.h_q) * C::DV * 2, lane, w,
+                              row_valid);
+        } else if (row_valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(orow + 8 * q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        }
+      } else if (row_valid) {
+#pragma unroll
+        for (int c = 0; c < C::OCOLS / C::OCH; ++c) {
 #pragma unroll
           for (int q8 = 0; q8 < C::OCH / 8; ++q8) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float lo = __uint_as_float(o[8 * q8 + 2 * e]) * f, hi = __uint_as_float(o[8 * q8 + 2 * e + 1]) * f;
+              const float lo = __uint_as_float(o[c][8 * q8 + 2 * e]) * f;
+              const float hi = __uint_as_float(o[c][8 * q8 + 2 * e + 1]) * f;
               w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
             }
-            *reinterpret_cast<uint4*>(orow + c + 8 * q8) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(orow + c * C::OCH + 8 * q8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
@@ -664,10 +732,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int c0 = col0 + e;
             if (c0 >= c_lo && c0 <= c_hi) mb = fmaxf(mb, __uint_as_float(sa[e]) * s_log2);
           }
-          sm.red[u & 1][grp][row] = mb;
+          ssm.red[u & 1][grp][row] = mb;
           act_groups_sync<C::NG>();
 #pragma unroll
-          for (int g = 0; g < C::NG; ++g) mb = fmaxf(mb, sm.red[u & 1][g][row]);
+          for (int g = 0; g < C::NG; ++g) mb = fmaxf(mb, ssm.red[u & 1][g][row]);
           // m is stale by at most 2^8: raise it (and rescale O) only past that
           const bool raise = mb > -INFINITY && (m == -INFINITY || mb > m + 8.0f);
           const float m_new = raise ? mb : m;
@@ -713,8 +781,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (softmax) {  // hand the row statistics to the epilogue warps
           ok = __all_sync(0xffffffffu, mbar_wait(&sm.stat_empty, (stat_cnt++ & 1) ^ 1, abort_flag));
           if (!ok) break;
-          sm.stat_l[grp][row] = l;
-          if (grp == 0) sm.stat_m[row] = m;
+          ssm.stat_l[grp][row] = l;
+          if (grp == 0) ssm.stat_m[row] = m;
           mbar_arrive(&sm.stat_full);
         }
       } else {
@@ -724,7 +792,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         pm = m;
       }
     }
-    if (ok && pend) ok = epilogue(pit, pl, pm);
+    if constexpr (!C::SEP_EPI) {
+      if (ok && pend) ok = epilogue(pit, pl, pm);
+    }
   } else if (C::SEP_EPI && warp >= C::EPI_WARP0) {
     // ------------------------------------------------ epilogue warps (two activation groups)
     const int quad = warp & 3;
@@ -734,6 +804,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (C::DT == DT_E4M3 && args.descale != nullptr) v_scale = args.descale[2];
     using OutT = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
     OutT* out = reinterpret_cast<OutT*>(args.out);
+    const bool out_v8 = (reinterpret_cast<uintptr_t>(args.out) & 31) == 0;
     uint32_t o_cnt = 0, stat_cnt = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -761,8 +832,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!ok) break;
         float l = 0.0f;
 #pragma unroll
-        for (int g = 0; g < C::NG; ++g) l += sm.stat_l[g][row];
-        const float m = sm.stat_m[row];
+        for (int g = 0; g < C::NG; ++g) l += ssm.stat_l[g][row];
+        const float m = ssm.stat_m[row];
         mbar_arrive(&sm.stat_empty);
         f = l > 0.0f ? v_scale / l : 0.0f;
         lse = l > 0.0f ? m * 0.6931471805599453f + __logf(l) : -INFINITY;
@@ -821,13 +892,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tc_fence_before();
             mbar_arrive(&sm.o_empty);
           }
-          if (row_valid) {
-            uint32_t w[16];
+          uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float lo = __uint_as_float(o[2 * e]) * f, hi = __uint_as_float(o[2 * e + 1]) * f;
-              w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
-            }
+          for (int e = 0; e < 16; ++e) {
+            const float lo = __uint_as_float(o[2 * e]) * f, hi = __uint_as_float(o[2 * e + 1]) * f;
+            w[e] = C::DT == DT_FP16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+          }
+          if (out_v8) {
+            store_rows64_paired(reinterpret_cast<uint8_t*>(orow + ch * 32), static_cast<size_t>(pb.h_q) * C::DV * 2,
+                                lane, w, row_valid);
+          } else if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);

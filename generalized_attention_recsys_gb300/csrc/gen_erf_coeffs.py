@@ -2,11 +2,19 @@
 
 GELU(z) = z * Phi(z), Phi(z) = erfc(-z / sqrt2) / 2.
 
-Forward (all FMA): erf(X v) ~ v * p(v^2) on v in [-1, 1], p of degree 8, X = 3
-(beyond |x| = 3 the kernel uses erf = +-1; erfc(3) = 2.2e-5), fitted by Lawson's
-algorithm (iteratively reweighted least squares converging to the minimax
-fit) on a dense grid; float32 Horner evaluation gives max |erf error| about
-2.4e-5, i.e. |Phi error| <= 1.2e-5.
+Forward (16-bit P): two evaluations of Phi, mixed per column so that the FMA
+and MUFU pipes share the work (act.cuh):
+
+  * polynomial (FMA pipe only): erf(X v) ~ v * p(v^2) with v = x / X clamped
+    to [-1, 1], p of degree 5, X chosen by scanning; the fit covers x in
+    [0, 7] with the clamp applied, so the tail beyond X is part of the
+    minimax error. Lawson's algorithm (iteratively reweighted least squares
+    converging to the minimax fit) on a dense grid.
+  * tanh form (one MUFU tanh per score): Phi(z) ~ (1 + tanh(a z + b z^3)) / 2.
+    a and b are fitted to atanh(2 Phi - 1) with weights dPhi/dy = 2 Phi (1 - Phi),
+    i.e. a linearised minimax fit of Phi itself (Lawson again), on |z| <= 6.
+
+The report gives each fit's max |Phi error| in float64.
 
 Backward (MUFU rcp + ex2): for x >= 0 the form of Abramowitz & Stegun,
 Handbook of Mathematical Functions, 7.1.25 (Hastings' approximation):
@@ -34,34 +42,53 @@ import numpy as np
 
 N_TERMS = 3
 X_MAX = 9.0
-POLY_X = 3.0
-POLY_TERMS = 9
+POLY_TERMS = 6
 
 
-def fit_poly(x_max: float, n: int, iters: int = 200) -> np.ndarray:
-    v = np.linspace(0.0, 1.0, 20001)
-    y = np.array([erf(x_max * vi) for vi in v])
+def fit_poly(x_clamp: float, n: int, iters: int = 300) -> tuple[np.ndarray, float]:
+    """erf(x) ~ v p(v^2), v = min(x / x_clamp, 1), minimax over x in [0, 7]; returns (p, max |erf error|)."""
+    x = np.linspace(0.0, 7.0, 30001)
+    y = np.array([erf(t) for t in x])
+    v = np.minimum(x / x_clamp, 1.0)
     u = v * v
     basis = np.stack([v * u ** i for i in range(n)], axis=1)
-    w = np.ones_like(v)
+    w = np.ones_like(x)
     for _ in range(iters):
         c, *_ = np.linalg.lstsq(basis * np.sqrt(w)[:, None], y * np.sqrt(w), rcond=None)
         err = np.abs(basis @ c - y)
         w = w * (err / err.max() + 1e-4)
         w /= w.mean()
-    return c
+    return c, float(np.abs(basis @ c - y).max())
 
 
-def poly_fp32_error(c: np.ndarray, x_max: float) -> float:
-    v = np.linspace(-1.3, 1.3, 200001).astype(np.float32)
-    vc = np.clip(v, -1, 1).astype(np.float32)
-    uu = (vc * vc).astype(np.float32)
-    p = np.float32(c[-1])
-    for ci in c[-2::-1]:
-        p = (p * uu + np.float32(ci)).astype(np.float32)
-    approx = (vc * p).astype(np.float32)
-    ref = np.array([erf(x_max * float(x)) for x in v])
-    return float(np.abs(approx - ref).max())
+def best_poly(n: int) -> tuple[float, np.ndarray, float]:
+    best = None
+    for xc in np.arange(2.0, 3.2, 0.05):
+        c, e = fit_poly(float(xc), n, 150)
+        if best is None or e < best[2]:
+            best = (float(xc), c, e)
+    c, e = fit_poly(best[0], n)
+    return best[0], c, e
+
+
+def fit_tanh_form(iters: int = 300) -> tuple[np.ndarray, float]:
+    """Phi(z) ~ (1 + tanh(a z + b z^3)) / 2: returns ((a, b), max |Phi error|)."""
+    z = np.linspace(1e-3, 6.0, 20001)
+    phi = np.array([0.5 * erfc(-t / np.sqrt(2.0)) for t in z])
+    y = np.arctanh(2.0 * phi - 1.0)
+    dphi = 2.0 * phi * (1.0 - phi)  # dPhi / dy
+    basis = np.stack([z, z ** 3], axis=1) * dphi[:, None]
+    target = y * dphi
+    w = np.ones_like(z)
+    for _ in range(iters):
+        c, *_ = np.linalg.lstsq(basis * np.sqrt(w)[:, None], target * np.sqrt(w), rcond=None)
+        err = np.abs(basis @ c - target)
+        w = w * (err / err.max() + 1e-4)
+        w /= w.mean()
+    zz = np.linspace(-12.0, 12.0, 240001)
+    ref = np.array([0.5 * erfc(-t / np.sqrt(2.0)) for t in zz])
+    approx = 0.5 * (1.0 + np.tanh(zz * (c[0] + c[1] * zz * zz)))
+    return c, float(np.abs(approx - ref).max())
 
 
 def fit(p: float, n: int, iters: int = 300) -> tuple[np.ndarray, float]:
@@ -109,10 +136,15 @@ def fp32_phi_error(p: float, c: np.ndarray) -> float:
 
 
 if __name__ == "__main__":
-    cp = fit_poly(POLY_X, POLY_TERMS)
-    print(f"// erf({POLY_X} v) ~ v * p(v^2), |v| <= 1; float32 max |erf error| {poly_fp32_error(cp, POLY_X):.2e}")
+    xc, cp, ep = best_poly(POLY_TERMS)
+    print(f"// erf(x) ~ v p(v^2), v = clamp(x / {xc:.2f}, -1, 1): max |erf error| {ep:.2e}, |Phi error| {ep / 2:.2e}")
+    print(f"constexpr float kGeluPolyX = {float(np.float32(xc))!r}f;")
     for i, ci in enumerate(cp):
         print(f"//   p[{i}] = {float(np.float32(ci))!r}f")
+    ct, et = fit_tanh_form()
+    print(f"// Phi(z) ~ (1 + tanh(a z + b z^3)) / 2: max |Phi error| {et:.2e}")
+    print(f"constexpr float kPhiTanhA = {float(np.float32(ct[0]))!r}f;")
+    print(f"constexpr float kPhiTanhB = {float(np.float32(ct[1]))!r}f;")
     p, c, e = best_fit(N_TERMS)
     print(f"// p = {p!r}; max |erfc error| {e:.2e}; float32 max |Phi error| {fp32_phi_error(p, c):.2e}")
     print(f"constexpr float kErfcP = {float(np.float32(p))!r}f;")

@@ -59,6 +59,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete. Returns false if
 // the abort flag is raised (by this or another thread) or the wait times out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -234,6 +249,76 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// Warp-wide forms: every lane of a converged warp executes the call and
+// elect.sync picks the one lane that issues. Descriptors and addresses are
+// then warp-uniform values, which keeps the per-MMA instruction count low
+// (about 20 issue cycles per MMA against about 48 for a lone lane that builds
+// each descriptor itself).
+__device__ __forceinline__ void mma_f16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, e;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, e;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, e;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, e;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Warp-wide commit (one elected lane).
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n"
+      " .reg .pred e;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// Descriptor of a tile at a byte offset from the one `base` describes (the
+// start address field is the low 14 bits, in 16-byte units; offsets stay
+// inside the 256 KB shared window, so nothing carries out of the field).
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t byte_off) {
+  return base + (byte_off >> 4);
+}
+
 // Arrive once on bar when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -302,6 +387,39 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- global stores
+
+// 32-byte store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Writes 64-byte row segments held one row per lane (w: this lane's 64
+// bytes) so that each store instruction covers 16 rows x 64 bytes instead
+// of 32 rows x 16 bytes: lanes 2p and 2p+1 swap 32-byte halves, then each
+// pair writes row 2p's segment and row 2p+1's segment with one 32-byte store
+// per lane each. All 32 lanes must call it (it shuffles). own: this lane's
+// segment (32-byte aligned); stride: bytes between consecutive rows;
+// valid: whether this lane's row is stored.
+__device__ __forceinline__ void store_rows64_paired(uint8_t* own, size_t stride, int lane, const uint32_t (&w)[16],
+                                                    bool valid) {
+  const bool odd = lane & 1;
+  uint32_t d1[8], d2[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? w[i] : w[8 + i], 1);
+    d1[i] = odd ? recv : w[i];      // even row: first half from the even lane, second from the odd one
+    d2[i] = odd ? w[8 + i] : recv;  // odd row likewise
+  }
+  const bool v_other = __shfl_xor_sync(0xffffffffu, valid, 1);
+  uint8_t* even_row = odd ? own - stride : own;
+  uint8_t* a1 = even_row + (odd ? 32 : 0);
+  if (odd ? v_other : valid) st_global_v8(a1, d1);
+  if (odd ? valid : v_other) st_global_v8(a1 + stride, d2);
+}
 
 // ---------------------------------------------------------------- packing
 

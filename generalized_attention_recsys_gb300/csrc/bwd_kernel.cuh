@@ -381,49 +381,50 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
-                     aDS = smem_u32(sDS);
+    // ------------------------------------------------ MMA issuer (whole warp; one elected lane issues)
+    {
+      // descriptors of every operand tile, built once; the K steps add byte offsets
+      const uint64_t dK_k = sdesc_sw128(smem_u32(sK), 16, 1024);            // K, K-major (A of S^T)
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(sK), C::BOX_BYTES, 1024);  // K, MN-major (B of dQ)
+      const uint64_t dV_k = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dQ_k = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), C::BOX_BYTES, 1024);
+      const uint64_t dDO_k = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t dDO_mn = sdesc_sw128(smem_u32(sDO), C::BOX_BYTES, 1024);
+      const uint64_t dDS_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
+      const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), C::BOX_BYTES, 1024);
       auto issue_s = [&](int st) {
-        const uint32_t q = aQ + st * C::Q_BYTES;
 #pragma unroll
         for (int k = 0; k < C::S_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
-          mma_f16_ss(tbase + C::T_S, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), C::IDESC_S,
-                     k > 0);
+          mma_f16_ss_w(tbase + C::T_S, sdesc_at(dK_k, off), sdesc_at(dQ_k, st * C::Q_BYTES + off), C::IDESC_S, k > 0);
         }
       };
       auto issue_dp = [&]() {
-        const uint32_t d = aDO;
 #pragma unroll
         for (int k = 0; k < C::DP_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
-          mma_f16_ss(tbase + C::T_DP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(d + off, 16, 1024),
-                     C::IDESC_S, k > 0);
+          mma_f16_ss_w(tbase + C::T_DP, sdesc_at(dV_k, off), sdesc_at(dDO_k, off), C::IDESC_S, k > 0);
         }
       };
       auto issue_dv = [&](bool acc) {  // dV += P^T dO (A = P^T from TMEM)
-        const uint32_t d = aDO;
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k)
-          mma_f16_ts(tbase + C::T_DV, tbase + C::T_S + pt_col<C>(k), sdesc_sw128(d + k * 2048, C::BOX_BYTES, 1024),
-                     C::IDESC_DV, (acc || k > 0) ? 1u : 0u);
+          mma_f16_ts_w(tbase + C::T_DV, tbase + C::T_S + pt_col<C>(k), sdesc_at(dDO_mn, k * 2048), C::IDESC_DV,
+                       (acc || k > 0) ? 1u : 0u);
       };
       auto issue_dq = [&]() {  // dQ = dS K
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k)
-          mma_f16_ss(tbase + C::T_DQ, sdesc_sw128(aDS + k * 2048, C::BOX_BYTES, 1024),
-                     sdesc_sw128(aK + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DQ, k > 0);
-        mma_commit(&sm.dq_full);
+          mma_f16_ss_w(tbase + C::T_DQ, sdesc_at(dDS_mn, k * 2048), sdesc_at(dK_mn, k * 2048), C::IDESC_DQ, k > 0);
+        mma_commit_w(&sm.dq_full);
       };
       auto issue_dk = [&](int st, bool acc) {  // dK += dS^T Q
-        const uint32_t q = aQ + st * C::Q_BYTES;
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
-          mma_f16_ss(tbase + C::T_DK, sdesc_sw128(aDS + off, 16, 1024),
-                     sdesc_sw128(q + k * 2048, C::BOX_BYTES, 1024), C::IDESC_DK, (acc || k > 0) ? 1u : 0u);
+          mma_f16_ss_w(tbase + C::T_DK, sdesc_at(dDS_k, off), sdesc_at(dQ_mn, st * C::Q_BYTES + k * 2048), C::IDESC_DK,
+                       (acc || k > 0) ? 1u : 0u);
         }
       };
       // Issue order per item (steps t = 0..n-1):
@@ -439,25 +440,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const bool s_first = bwd_s_first(args.act);
       uint32_t kv_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, dqe = 0, acce = 0;
       bool ok = true;
+      // every lane waits; the warp goes on only if all of them succeeded
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
       auto issue_s_at = [&](uint32_t it_idx) -> bool {
         const int st = it_idx % C::Q_STAGES;
-        if (!mbar_wait(&sm.q_full[st], (it_idx / C::Q_STAGES) & 1, abort_flag)) return false;
+        if (!wait_all(&sm.q_full[st], (it_idx / C::Q_STAGES) & 1)) return false;
         tc_fence_after();
         issue_s(st);
-        mma_commit(&sm.s_full);
+        mma_commit_w(&sm.s_full);
         return true;
       };
       auto issue_dp_dv_at = [&](uint32_t it_idx, bool first) -> bool {
-        if (!mbar_wait(&sm.dq_empty, (dqe++ & 1) ^ 1, abort_flag)) return false;
-        if (!mbar_wait(&sm.do_full, it_idx & 1, abort_flag)) return false;
+        if (!wait_all(&sm.dq_empty, (dqe++ & 1) ^ 1)) return false;
+        if (!wait_all(&sm.do_full, it_idx & 1)) return false;
         tc_fence_after();
         issue_dp();
-        mma_commit(&sm.dp_full);
-        if (!mbar_wait(&sm.p_full, p_cnt++ & 1, abort_flag)) return false;
-        if (first && !mbar_wait(&sm.acc_empty, (acce++ & 1) ^ 1, abort_flag)) return false;
+        mma_commit_w(&sm.dp_full);
+        if (!wait_all(&sm.p_full, p_cnt++ & 1)) return false;
+        if (first && !wait_all(&sm.acc_empty, (acce++ & 1) ^ 1)) return false;
         tc_fence_after();
         issue_dv(!first);
-        mma_commit(&sm.do_empty);  // dV is the last reader of this dO tile
+        mma_commit_w(&sm.do_empty);  // dV is the last reader of this dO tile
         return true;
       };
       for (int round = 0; ok; ++round) {
@@ -465,13 +470,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (pos >= n_work) break;
         const BwdItem it = bwd_decode(args, pos);
         if (it.nsteps == 0) continue;
-        ok = mbar_wait(&sm.kv_full, kv_cnt++ & 1, abort_flag);
+        ok = wait_all(&sm.kv_full, kv_cnt++ & 1);
         if (ok) ok = issue_s_at(qd_it);
         if (ok) ok = issue_dp_dv_at(qd_it, true);
         for (int s = 0; s < it.nsteps && ok; ++s) {
           const int st = qd_it % C::Q_STAGES;
           const bool more = s + 1 < it.nsteps;
-          ok = mbar_wait(&sm.ds_full, ds_cnt++ & 1, abort_flag);
+          ok = wait_all(&sm.ds_full, ds_cnt++ & 1);
           if (!ok) break;
           if (s_first && more && !issue_s_at(qd_it + 1)) {
             ok = false;
@@ -484,11 +489,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             break;
           }
           issue_dk(st, s > 0);
-          mma_commit(&sm.q_empty[st]);
+          mma_commit_w(&sm.q_empty[st]);
           ++qd_it;
           if (!more) {
-            mma_commit(&sm.acc_full);
-            mma_commit(&sm.kv_empty);
+            mma_commit_w(&sm.acc_full);
+            mma_commit_w(&sm.kv_empty);
           } else {
             ok = issue_dp_dv_at(qd_it, false);
           }

@@ -155,7 +155,7 @@ int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int
 }
 
 // Work list: entries (b, blk) sorted by cost, heaviest first (counting sort
-// over cost buckets). mode 0: blk = 256-row query item, cost = KV blocks it
+// over cost buckets). mode 0: blk = 128-row query item, cost = KV blocks it
 // visits; mode 1: blk = 128-row key block, cost = query blocks that see it.
 constexpr int kBuckets = 2048;
 
@@ -363,6 +363,10 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.dq_acc = dq_acc;
   a.dq_part = dq_part;
   a.drow = drow;
+  // one key block per sequence: each dQ row has a single producer, written in
+  // place (deterministic by construction, so it serves both modes)
+  a.dq_mode = max_k <= kTileK ? DQ_DIRECT : (deterministic ? DQ_SLICES : DQ_ACCUMULATE);
+  a.n_kblocks = (max_k + kTileK - 1) / kTileK;
   a.d_qk = s->d_qk;
   a.d_v = s->d_v;
   a.dtype = s->dtype;

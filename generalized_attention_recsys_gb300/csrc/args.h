@@ -19,6 +19,15 @@ struct FwdArgs {
   int* status;  // device status word; a bounded wait that gave up writes 5 (timeout)
 };
 
+// How the backward produces dQ.
+//   DQ_ACCUMULATE: TMA reduce-adds into an fp32 accumulator, converted after.
+//   DQ_SLICES:     deterministic mode: each key block's dQ tile into its own
+//                  fp32 slice, added in key-block order after.
+//   DQ_DIRECT:     every sequence has at most one 128-row key block
+//                  (max_k <= 128), so each dQ row has exactly one producer
+//                  and the kernel writes it in the output type directly.
+enum DqMode : int { DQ_ACCUMULATE = 0, DQ_SLICES = 1, DQ_DIRECT = 2 };
+
 struct BwdArgs {
   Problem pb;
   int act;
@@ -35,6 +44,8 @@ struct BwdArgs {
   float* dq_part;    // deterministic mode: fp32 [ceil(max_k / 128), total_q, h_q, dqk], one slice per
                      // key block; NULL otherwise
   float* drow;       // workspace: softmax rowsum(dO * O), [h_q, total_q]
+  int dq_mode;       // DQ_ACCUMULATE, DQ_SLICES (deterministic) or DQ_DIRECT
+  int n_kblocks;     // ceil(max_k / 128): key blocks a sequence may have (checked on the device)
   int d_qk, d_v, dtype;
 };
 

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "act.cuh"
 #include "args.h"
 
 namespace gdpa {
@@ -29,13 +30,40 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 template <>
 __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 
-// Zero the dQ accumulator; softmax: drow[h, t] = sum_d dO[t, h, d] * O[t, h, d].
+// Zero the dQ accumulator (n4 float4s; 0 when there is none); softmax:
+// drow[h, t] = sum_d dO[t, h, d] * O[t, h, d]. With direct dQ (zero_dq set),
+// the rows of query blocks that no work item visits are zeroed in dq itself
+// (every sequence has at most one key block, covering the query blocks that
+// query_range gives; the kernel writes the rest).
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_prep(float4* acc, size_t n4, const T* out, const T* dout, float* drow,
-                                                int total_q, int h_q, int d_v) {
+                                                int total_q, int h_q, int d_v, Problem pb, T* zero_dq, int d_qk) {
   const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
   const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = tid; i < n4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (zero_dq != nullptr) {
+    const size_t row_elems = static_cast<size_t>(h_q) * d_qk;  // one token: every head
+    for (int b = static_cast<int>(tid / 32); b < pb.batch; b += static_cast<int>(nthr / 32)) {
+      int qs, lq, ks, lk;
+      seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
+      seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
+      int r0 = 0, r1 = 0;  // covered rows [r0, r1)
+      int rmin, rmax;
+      if (lq > 0 && lk > 0 && query_range(0, lk - 1, lq, lk, pb.causal, pb.window, rmin, rmax)) {
+        r0 = (rmin / kTileQ) * kTileQ;
+        r1 = min(lq, (rmax / kTileQ + 1) * kTileQ);
+      }
+      // [0, r0) and [r1, lq) are contiguous token ranges
+      for (int part = 0; part < 2; ++part) {
+        const int a0 = part == 0 ? 0 : r1, a1 = part == 0 ? r0 : lq;
+        if (a1 <= a0) continue;
+        T* base = zero_dq + static_cast<size_t>(qs + a0) * row_elems;
+        const size_t n = static_cast<size_t>(a1 - a0) * row_elems;  // multiple of 8 elements (16 bytes)
+        for (size_t i = (tid & 31) * 8; i < n; i += 32 * 8)
+          *reinterpret_cast<uint4*>(base + i) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
   if (drow == nullptr) return;
   const size_t warp = tid / 32, nwarps = nthr / 32;
   const int lane = threadIdx.x & 31;
@@ -78,7 +106,7 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
 // covered the row's 128-row query block (the same query_range test the work
 // items use, so only written slices are read). One warp per row.
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Problem pb, int d, T* dq) {
+__global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Problem pb, int d, int n_slices, T* dq) {
   const int lane = threadIdx.x & 31;
   const size_t nwarps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
   const size_t rows = static_cast<size_t>(pb.total_q) * pb.h_q;
@@ -101,7 +129,9 @@ __global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Probl
     seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
     const int qb = (t - qs) / kTileQ;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};  // columns lane, lane + 32, ... (d <= 128)
-    const int nkv = lk > 0 ? (lk + kTileK - 1) / kTileK : 0;
+    // the workspace holds n_slices; a longer key sequence (max_k understated)
+    // was reported by the main kernel, which wrote no slice beyond them
+    const int nkv = min(lk > 0 ? (lk + kTileK - 1) / kTileK : 0, n_slices);
     for (int j = 0; j < nkv; ++j) {
       const int k0 = j * kTileK, k1 = min(k0 + kTileK, lk) - 1;
       int rmin, rmax;
@@ -130,18 +160,21 @@ __global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T*
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdq, const BwdArgs& a, int grid, cudaStream_t stream, cudaEvent_t before,
                        cudaEvent_t after) {
-  const bool ordered = a.dq_part != nullptr;  // deterministic mode: no accumulator to clear
-  const size_t n4 = ordered ? 0 : static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4;
+  // only the accumulating mode has an accumulator to clear
+  const size_t n4 = a.dq_mode == DQ_ACCUMULATE ? static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4 : 0;
+  const bool direct = a.dq_mode == DQ_DIRECT;
   const int eg = grid * 8;  // elementwise kernels: 8 blocks of 256 per SM
-  float* drow = a.act == 9 ? a.drow : nullptr;
+  float* drow = a.act == ACT_SOFTMAX ? a.drow : nullptr;
   if (a.dtype == DT_FP16)
     bwd_prep<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<float4*>(a.dq_acc), n4,
                                              static_cast<const __half*>(a.out), static_cast<const __half*>(a.dout),
-                                             drow, a.pb.total_q, a.pb.h_q, a.d_v);
+                                             drow, a.pb.total_q, a.pb.h_q, a.d_v, a.pb,
+                                             direct ? static_cast<__half*>(a.dq) : nullptr, a.d_qk);
   else
     bwd_prep<__nv_bfloat16><<<eg, 256, 0, stream>>>(
         reinterpret_cast<float4*>(a.dq_acc), n4, static_cast<const __nv_bfloat16*>(a.out),
-        static_cast<const __nv_bfloat16*>(a.dout), drow, a.pb.total_q, a.pb.h_q, a.d_v);
+        static_cast<const __nv_bfloat16*>(a.dout), drow, a.pb.total_q, a.pb.h_q, a.d_v, a.pb,
+        direct ? static_cast<__nv_bfloat16*>(a.dq) : nullptr, a.d_qk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (before) cudaEventRecord(before, stream);
@@ -153,11 +186,13 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   }
   if (e != cudaSuccess) return e;
   if (after) cudaEventRecord(after, stream);
-  if (ordered) {
+  if (direct) return cudaSuccess;  // dQ is already in place
+  if (a.dq_mode == DQ_SLICES) {
     if (a.dtype == DT_FP16)
-      bwd_post_ordered<__half><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk, static_cast<__half*>(a.dq));
+      bwd_post_ordered<__half><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk, a.n_kblocks,
+                                                     static_cast<__half*>(a.dq));
     else
-      bwd_post_ordered<__nv_bfloat16><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk,
+      bwd_post_ordered<__nv_bfloat16><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk, a.n_kblocks,
                                                              static_cast<__nv_bfloat16*>(a.dq));
     return cudaGetLastError();
   }

@@ -45,9 +45,13 @@
 
 namespace gdpa {
 
-template <int DQK_, int DV_, int DT_>
+// DIRECT_DQ_: the dQ drain writes each tile in the output type (one key
+// block per sequence); otherwise it adds into fp32 (accumulator or slices).
+// Separate instantiations, so neither drain carries the other's registers.
+template <int DQK_, int DV_, int DT_, bool DIRECT_DQ_ = false>
 struct BwdCfg {
   static constexpr int DQK = DQK_, DV = DV_, DT = DT_;
+  static constexpr bool DIRECT_DQ = DIRECT_DQ_;
   static_assert(DT == DT_BF16 || DT == DT_FP16, "backward takes 16-bit inputs");
   static_assert(DQK <= 128 && DV <= 128, "backward TMEM plan holds head dims up to 128");
   static constexpr int BOX_ELEMS = 64;
@@ -615,12 +619,57 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_full, dq_cnt++ & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        if (q0 + quad * 32 >= it.lq) {  // this warp's 32 rows lie wholly past the sequence: nothing to add
+        // a key block the caller's max_k does not allow: its slice (or, with
+        // one producer per row, its rows) would lie outside what the workspace
+        // and the mode were sized for, so report the violated precondition
+        // and write nothing
+        const bool kb_ok = it.k0 / kTileK < args.n_kblocks;
+        if (!kb_ok && lane == 0 && quad == 0) atomicExch(args.status, 1);
+        if (!kb_ok || q0 + quad * 32 >= it.lq) {  // nothing to add for this warp's 32 rows
           tc_fence_before();
           mbar_arrive(&sm.dq_empty);
           continue;
         }
-        if (args.dq_part != nullptr) {
+        if constexpr (C::DIRECT_DQ) {
+          // the only key block of the sequence: dQ rows in the output type,
+          // 32 columns a chunk, written as paired 32-byte stores
+          using T = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
+          T* drow_out = reinterpret_cast<T*>(args.dq) +
+                        (static_cast<size_t>(it.q_start + q0 + row) * pb.h_q + h) * C::DQK;
+          const bool v8 = (reinterpret_cast<uintptr_t>(args.dq) & 31) == 0;
+          const size_t stride = static_cast<size_t>(pb.h_q) * C::DQK * sizeof(T);
+#pragma unroll
+          for (int pr = 0; pr < NPAIR; ++pr) {
+            const int c0 = 2 * pr;
+            uint32_t a[32], b[32];
+            tmem_ld32(t_dq + c0 * 32, a);
+            if (c0 + 1 < NCH) tmem_ld32(t_dq + (c0 + 1) * 32, b);
+            tmem_ld_wait(a);
+            if (c0 + 1 < NCH) tmem_ld_wait(b);
+            if (pr == NPAIR - 1) {
+              tc_fence_before();
+              mbar_arrive(&sm.dq_empty);  // every TMEM read of this tile is done
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              if (c0 + half >= NCH) break;
+              const uint32_t(&o)[32] = half == 0 ? a : b;
+              uint32_t w[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) w[e] = pack16<C::DT>(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+              T* dst = drow_out + (c0 + half) * 32;
+              if (v8) {
+                store_rows64_paired(reinterpret_cast<uint8_t*>(dst), stride, lane, w, valid);
+              } else if (valid) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                  reinterpret_cast<uint4*>(dst)[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+              }
+            }
+          }
+          continue;
+        } else {
+        if (args.dq_mode == DQ_SLICES) {
           // deterministic mode: this key block's dQ tile goes to its own slice; a
           // later kernel adds the slices in key-block order
           float* dst = args.dq_part + ((static_cast<size_t>(it.k0 / kTileK) * pb.total_q + it.q_start + q0 + row) *
@@ -687,6 +736,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           __syncwarp();
         }
         if (lane == 0) reduce_pair(2 * (NPAIR - 1));
+        }  // not C::DIRECT_DQ
       }
     }
     if (lane == 0) bulk_wait_group_all();
@@ -709,11 +759,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 }
 
-template <int DQK, int DV, int DT>
-cudaError_t launch_bwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
-                           cudaStream_t stream) {
-  using C = BwdCfg<DQK, DV, DT>;
+template <int DQK, int DV, int DT, bool DIRECT>
+cudaError_t launch_bwd_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                              cudaStream_t stream) {
+  using C = BwdCfg<DQK, DV, DT, DIRECT>;
   auto kern = gdpa_bwd_kernel<C>;
   // the per-role register split assumes 128 registers a thread at launch
   cudaFuncAttributes fa;
@@ -722,6 +772,14 @@ cudaError_t launch_bwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
+}
+
+template <int DQK, int DV, int DT>
+cudaError_t launch_bwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                           cudaStream_t stream) {
+  if (a.dq_mode == DQ_DIRECT) return launch_bwd_kernel<DQK, DV, DT, true>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  return launch_bwd_kernel<DQK, DV, DT, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
 }
 
 }  // namespace gdpa

@@ -45,7 +45,10 @@
  * is bounded; a wait that gives up records GDPA_ERR_TIMEOUT in a per-device
  * status word that gdpa_get_status() returns. cu_seqlens consistency
  * (monotone, lengths <= max_seqlen, cu[batch] = total) is a caller
- * precondition and is not checked on the device.
+ * precondition. The backward checks the one part of it that sizes its
+ * writes: a key block beyond max_seqlen_k records GDPA_ERR_INVALID in the
+ * status word and that block writes no dq (the rest of the call still
+ * runs, so dq is then incomplete).
  */
 #ifndef GDPA_H_
 #define GDPA_H_
@@ -137,7 +140,10 @@ int gdpa_fwd(const gdpa_shape* shape, const void* q, const void* k, const void* 
  * deterministic != 0 each key block writes its own fp32 slice and a final
  * kernel adds the slices in key-block order, so dq is bitwise reproducible
  * (at the cost of the slices' memory, see gdpa_workspace_bytes, and their
- * HBM traffic). FA's flash_attn_varlen_func(deterministic=...) is the model. */
+ * HBM traffic). FA's flash_attn_varlen_func(deterministic=...) is the model.
+ * When max_seqlen_k <= 128 every sequence has one key block, so each dq row
+ * has a single producer: the kernel then writes dq directly in the output
+ * type (no accumulator, reproducible in either mode). */
 int gdpa_bwd(const gdpa_shape* shape, const void* q, const void* k, const void* v,
              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
              int max_seqlen_k, int act, float scale, int causal, int window, const void* out,
@@ -145,8 +151,9 @@ int gdpa_bwd(const gdpa_shape* shape, const void* q, const void* k, const void* 
              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device-side status of
- * the current device (GDPA_OK or GDPA_ERR_TIMEOUT), or GDPA_ERR_CUDA if
- * the synchronisation itself failed. */
+ * the current device (GDPA_OK, GDPA_ERR_TIMEOUT, or GDPA_ERR_INVALID for a
+ * key block beyond max_seqlen_k in the backward), or GDPA_ERR_CUDA if the
+ * synchronisation itself failed. */
 int gdpa_get_status(void* stream);
 
 /* Static, human-readable text for a status code. */

@@ -190,13 +190,37 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int c = kBuckets - 1; c >= 0; --c) {
-      const int t = hist[c];
-      hist[c] = run;
-      run += t;
+  // exclusive prefix over the buckets, heaviest first: each of the 1024
+  // threads owns two consecutive positions of that order; a warp scan, then
+  // a scan of the 32 warp totals
+  static_assert(kBuckets == 2 * 1024, "two buckets a thread");
+  __shared__ int warp_sum[32];
+  const int c0 = kBuckets - 1 - 2 * static_cast<int>(threadIdx.x), c1 = c0 - 1;
+  const int h0 = hist[c0], h1 = hist[c1];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = h0 + h1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = warp_sum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
     }
+    warp_sum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - (h0 + h1) + (wid > 0 ? warp_sum[wid - 1] : 0);
+  hist[c0] = excl;
+  hist[c1] = excl + h0;
+  if (threadIdx.x == 0) {
+    const int run = warp_sum[31];
     wl->count = run < cap ? run : cap;
   }
   __syncthreads();

@@ -765,11 +765,18 @@ cudaError_t launch_bwd_kernel(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               cudaStream_t stream) {
   using C = BwdCfg<DQK, DV, DT, DIRECT>;
   auto kern = gdpa_bwd_kernel<C>;
-  // the per-role register split assumes 128 registers a thread at launch
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < 128) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  // once per instantiation and device (attributes are per device)
+  static thread_local int attr_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (attr_dev != dev) {
+    // the per-role register split assumes 128 registers a thread at launch
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < 128) return cudaErrorInvalidConfiguration;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }

@@ -942,8 +942,15 @@ cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           int grid, cudaStream_t stream) {
   using C = FwdCfg<DQK, DV, DT, NG, SOFTMAX>;
   auto kern = gdpa_fwd_kernel<C>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  // once per instantiation and device (the attribute is per device)
+  static thread_local int attr_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (attr_dev != dev) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

@@ -50,10 +50,10 @@ def test_head_dims(dims, act):
     _check(inputs.custom(5, 4, 2, dims[0], dims[1], lens, lens, act, causal=True, seed=13), f"dims={dims}")
 
 
-@pytest.mark.parametrize("act", ["gelu_tanh", "relu2"])
+@pytest.mark.parametrize("act", ALL_ACTS)
 def test_fp16(act):
     lens = [129, 256, 7, 400]
-    _check(inputs.custom(4, 2, 2, 128, 128, lens, lens, act, dtype="fp16", seed=14), "fp16")
+    _check(inputs.custom(4, 2, 2, 128, 128, lens, lens, act, dtype="fp16", seed=14), f"fp16 {act}")
 
 
 def test_empty_and_unseen_blocks_give_zero_gradients():

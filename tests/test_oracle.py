@@ -318,8 +318,9 @@ def _brute(lens_q, lens_k, hq, hkv, dqk, dv, act, scale, causal, window, seed):
 def test_exact_rational_brute_force(act, causal, window):
     lens_q, lens_k = [3, 0, 4], [4, 2, 4]
     scale = Fraction(1, 2)
-    q, k, v, do, out_e, dq_e, dk_e, dv_e = _brute(lens_q, lens_k, 4, 2, 3, 2, act, scale,
-                                                  causal, window, seed=hash((act, causal, window)) % 1000)
+    # a fixed seed per case (string hashing is salted per process, so no hash())
+    seed = 100 * ["identity", "relu", "relu2", "leaky_relu", "hardswish"].index(act) + 10 * int(causal) + max(window, 0)
+    q, k, v, do, out_e, dq_e, dk_e, dv_e = _brute(lens_q, lens_k, 4, 2, 3, 2, act, scale, causal, window, seed=seed)
     cu_q, cu_k = _cu(lens_q), _cu(lens_k)
     out, _ = gdpa_fwd(q, k, v, cu_q, cu_k, 3, 4, 4, act, float(scale), causal, window)
     dq, dk, dv = gdpa_bwd(q, k, v, do, cu_q, cu_k, 3, 4, 4, act, float(scale), causal, window)

@@ -6,16 +6,16 @@ that forbids allocations after start-up). gdpa_fwd_noalloc serves them by
 keeping the forward's scratch (the work list) in a fixed array inside the
 library. This test calls it through the C ABI twice in a row, on two
 different problems, and checks each result against the workspace-taking
-gdpa_fwd within the forward tolerance the other tests use. It lives in a
-file that pytest collects last so that a stop-at-first-failure run has
-already run every other test.
+gdpa_fwd and against the float64 oracle, within the forward tolerance the
+other tests use. It lives in a file that pytest collects last so that a
+stop-at-first-failure run has already run every other test.
 """
 
 import pytest
 import torch
 
 from generalized_attention_recsys_gb300 import _lib, inputs
-from gpu_util import FWD_TOL, assert_close, ensure_built, max_lens, to_dev
+from gpu_util import FWD_TOL, assert_close, ensure_built, max_lens, ref_fwd, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -41,3 +41,5 @@ def test_noalloc_forward_matches_gdpa_fwd_on_two_calls_in_a_row():
     for inp in (first, second):
         got, ref = _both(inp)
         assert_close(got, ref, FWD_TOL, "gdpa_fwd_noalloc vs gdpa_fwd")
+        oracle_out, _ = ref_fwd(inp)
+        assert_close(got, oracle_out, FWD_TOL, "gdpa_fwd_noalloc vs the oracle")

@@ -3,6 +3,11 @@
 Each translation unit compiles in its own nvcc process (in parallel), then
 one link step produces ``libgdpa.so`` next to this file. A unit is rebuilt
 only when it or a header under csrc/ or include/ is newer than its object.
+
+``build(test_hooks=True)`` produces ``libgdpa_test.so`` instead, compiled
+with GDPA_TEST_HOOKS: device waits give up after 1 ms and the extra entry
+point gdpa_test_set_skip() makes one chosen mbarrier arrive be skipped, so
+that tests can make a wait run out. Only tests load it.
 """
 
 from __future__ import annotations
@@ -19,6 +24,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdpa.so")
+OBJ_TEST = os.path.join(PKG, "_build_test")
+LIB_TEST = os.path.join(PKG, "libgdpa_test.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -37,11 +44,11 @@ def _headers_mtime() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def _compile(src: str, nvcc: str, hdr_t: float, verbose: bool) -> str:
-    obj = os.path.join(OBJ, os.path.basename(src).replace(".cu", ".o"))
+def _compile(src: str, nvcc: str, hdr_t: float, verbose: bool, obj_dir: str, extra: list[str]) -> str:
+    obj = os.path.join(obj_dir, os.path.basename(src).replace(".cu", ".o"))
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_t):
         return obj
-    cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd), flush=True)
@@ -53,22 +60,24 @@ def _compile(src: str, nvcc: str, hdr_t: float, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, jobs: int | None = None) -> str:
+def build(verbose: bool = False, jobs: int | None = None, test_hooks: bool = False) -> str:
     nvcc = _nvcc()
-    os.makedirs(OBJ, exist_ok=True)
+    obj_dir, lib = (OBJ_TEST, LIB_TEST) if test_hooks else (OBJ, LIB)
+    extra = ["-DGDPA_TEST_HOOKS"] if test_hooks else []
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_t = _headers_mtime()
     with ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, nvcc, hdr_t, verbose), srcs))
+        objs = list(ex.map(lambda s: _compile(s, nvcc, hdr_t, verbose, obj_dir, extra), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + ".tmp"
+    if not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+        tmp = lib + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lrt", "-lpthread", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -240,6 +240,11 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
 
 thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
 
+#ifdef GDPA_TEST_HOOKS
+// test-only builds: the step at which CTA 0 skips one arrive ([0] forward, [1] backward; -1 = none)
+int g_test_skip[2] = {-1, -1};
+#endif
+
 void mark(cudaEvent_t ev, cudaStream_t stream) {
   if (ev) cudaEventRecord(ev, stream);
 }
@@ -320,6 +325,9 @@ int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.lse = lse;
   a.work = wl;
   a.status = status;
+#ifdef GDPA_TEST_HOOKS
+  a.test_skip_step = g_test_skip[0];
+#endif
   cudaError_t e;
   mark(t_ev_before, stream);
   switch (s->d_qk) {
@@ -387,6 +395,9 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.dq_acc = dq_acc;
   a.dq_part = dq_part;
   a.drow = drow;
+#ifdef GDPA_TEST_HOOKS
+  a.test_skip_step = g_test_skip[1];
+#endif
   // one key block per sequence: each dQ row has a single producer, written in
   // place (deterministic by construction, so it serves both modes)
   a.dq_mode = max_k <= kTileK ? DQ_DIRECT : (deterministic ? DQ_SLICES : DQ_ACCUMULATE);
@@ -432,6 +443,17 @@ const char* gdpa_error_string(int s) {
 }
 
 int gdpa_num_sms(void) { return sm_count(); }
+
+#ifdef GDPA_TEST_HOOKS
+// Test-only builds: from the next call on, CTA 0 of the forward (kernel 0) or
+// backward (kernel 1) skips one mbarrier arrive at `step` (-1: none), so that
+// a bounded wait runs out and the call ends with GDPA_ERR_TIMEOUT.
+int gdpa_test_set_skip(int kernel, int step) {
+  if (kernel < 0 || kernel > 1) return GDPA_ERR_INVALID;
+  g_test_skip[kernel] = step;
+  return GDPA_OK;
+}
+#endif
 
 int gdpa_set_profile_events(void* before_main, void* after_main) {
   t_ev_before = static_cast<cudaEvent_t>(before_main);

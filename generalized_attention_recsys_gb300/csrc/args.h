@@ -17,6 +17,9 @@ struct FwdArgs {
   float* lse;            // [h_q, total_q] (softmax)
   const WorkList* work;
   int* status;  // device status word; a bounded wait that gave up writes 5 (timeout)
+#ifdef GDPA_TEST_HOOKS
+  int test_skip_step;  // test-only builds: CTA 0's activation warps skip the P-full arrive of this step
+#endif
 };
 
 // How the backward produces dQ.
@@ -44,6 +47,9 @@ struct BwdArgs {
   float* dq_part;    // deterministic mode: fp32 [ceil(max_k / 128), total_q, h_q, dqk], one slice per
                      // key block; NULL otherwise
   float* drow;       // workspace: softmax rowsum(dO * O), [h_q, total_q]
+#ifdef GDPA_TEST_HOOKS
+  int test_skip_step;  // test-only builds: CTA 0's elementwise warps skip the dS-full arrive of this step
+#endif
   int dq_mode;       // DQ_ACCUMULATE, DQ_SLICES (deterministic) or DQ_DIRECT
   int n_kblocks;     // ceil(max_k / 128): key blocks a sequence may have (checked on the device)
   int d_qk, d_v, dtype;

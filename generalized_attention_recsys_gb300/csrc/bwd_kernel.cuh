@@ -128,8 +128,10 @@ struct BwdSmem {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_full, acc_empty;
+  uint64_t drain;    // abort path: every MMA the issuing warp issued has completed
   uint32_t tmem_base;
   int abort_flag;
+  int drain_failed;  // abort path: a role's in-flight work did not land in time
 };
 
 template <int DT>
@@ -316,6 +318,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(&sm.dq_empty, 128);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, 128 * C::NG);
+    mbar_init(&sm.drain, 1);
+    sm.drain_failed = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // the dO tile of every step, so the next item's first tiles load while
     // the current item still holds K and V.
     if (lane == 0) {
-      uint32_t kv_cnt = 0, st_it = 0;
+      uint32_t kv_cnt = 0, st_it = 0, issued = 0;  // issued: K/V, Q or dO loads of this thread
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int pos = zigzag_pos(round, blockIdx.x, G);
@@ -361,6 +365,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load_3d(sK + bx * C::BOX_BYTES, &tm_k, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
           for (int bx = 0; bx < C::V_BOXES; ++bx)
             tma_load_3d(sV + bx * C::BOX_BYTES, &tm_v, &sm.kv_full, bx * 64, it.g, it.k_start + it.k0);
+          issued = kv_cnt;
           continue;
         }
         for (int s = 0; s < it.nsteps && ok; ++s, ++st_it) {
@@ -374,14 +379,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int bx = 0; bx < C::QK_BOXES; ++bx)
               tma_load_3d(sQ + st * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[st], bx * 64, h,
                           it.q_start + q0);
+            issued = st_it + 1;
           } else {
             ok = mbar_wait(&sm.do_empty, (st_it & 1) ^ 1, abort_flag);
             if (!ok) break;
             mbar_arrive_expect_tx(&sm.do_full, C::DO_BYTES);
             for (int bx = 0; bx < C::V_BOXES; ++bx)
               tma_load_3d(sDO + bx * C::BOX_BYTES, &tm_do, &sm.do_full, bx * 64, h, it.q_start + q0);
+            issued = st_it + 1;
           }
         }
+      }
+      if (*abort_flag) {  // let this thread's last loads land before the tiles go away
+        bool landed = true;
+        if (warp == 0 && issued > 0) landed = mbar_wait_timed(&sm.kv_full, (issued - 1) & 1, kDrainTimeoutNs);
+        if (warp == 2)
+          for (uint32_t i = 0; i < issued && i < static_cast<uint32_t>(C::Q_STAGES); ++i) {
+            const uint32_t n = issued - 1 - i;
+            landed = mbar_wait_timed(&sm.q_full[n % C::Q_STAGES], (n / C::Q_STAGES) & 1, kDrainTimeoutNs) && landed;
+          }
+        if (warp == 3 && issued > 0) landed = mbar_wait_timed(&sm.do_full, (issued - 1) & 1, kDrainTimeoutNs);
+        if (!landed) sm.drain_failed = 1;
       }
     }
   } else if (warp == 1) {
@@ -503,6 +521,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
       }
+      if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
+        mma_commit_w(&sm.drain);
+        if (!__all_sync(0xffffffffu, mbar_wait_timed(&sm.drain, 0, kDrainTimeoutNs)) && lane == 0)
+          sm.drain_failed = 1;
+      }
     }
   } else if (warp >= C::ACT_WARP0 && warp < C::DRAIN_WARP0) {
     // ------------------------------------------------ elementwise groups + dK/dV epilogue
@@ -567,6 +590,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           bwd_pass2<C, false>(t_lane, sDS, row, w, bwd_k.scale, drow, col_base, col_max);
         fence_async_shared();
         tc_fence_before();
+#ifdef GDPA_TEST_HOOKS
+        if (!(blockIdx.x == 0 && static_cast<int>(s_cnt - 1) == args.test_skip_step))
+#endif
         mbar_arrive(&sm.ds_full);
       }
       if (!ok) break;
@@ -743,11 +769,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 
   // ------------------------------------------------ teardown
+  // After an abort each role above has waited (time-bounded) for its own
+  // TMA loads, MMAs and bulk reduce-adds in flight; only if one of those
+  // waits gave up does the CTA also wait a fixed 1 ms before TMEM and shared
+  // memory go away.
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
-    const unsigned long long t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 1000000ull) {
+    if (sm.drain_failed) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) {
+      }
     }
     if (threadIdx.x == 0) atomicExch(args.status, 5);
   }

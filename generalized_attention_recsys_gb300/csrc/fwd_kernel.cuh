@@ -191,8 +191,11 @@ struct FwdSmem {
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, o_empty, pv_done[2];
   uint64_t stat_full, stat_empty;
+  uint64_t red_full[2];  // softmax: every group's partial row max of step u is in red[u % 2]
+  uint64_t drain[2];     // abort path: MMAs issued by the S / PV warp have completed
   uint32_t tmem_base;
   int abort_flag;
+  int drain_failed;      // abort path: a role's in-flight work did not land in time
 };
 
 // Softmax only: the row statistics the activation groups exchange.
@@ -372,12 +375,6 @@ __device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint
 #undef GDPA_ACT_CASE
 }
 
-// Named barrier over the activation groups (warps 4 .. 4 + 4 NG - 1).
-template <int NG>
-__device__ __forceinline__ void act_groups_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(128 * NG) : "memory");
-}
-
 // ---------------------------------------------------------------- the kernel
 
 template <class C>
@@ -425,6 +422,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(&sm.stat_empty, 128);
     mbar_init(&sm.pv_done[0], 1);
     mbar_init(&sm.pv_done[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.red_full[i], 128 * C::NG);
+      mbar_init(&sm.drain[i], 1);
+    }
+    sm.drain_failed = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -444,7 +446,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer: Q tiles and the K ring
     if (lane == 0) {
-      uint32_t k_it = 0;
+      uint32_t k_it = 0, q_loads = 0;
       StepCursor kc, qc;
       kc.start(args, n_work);
       qc.start(args, n_work);
@@ -465,6 +467,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int bx = 0; bx < C::QK_BOXES; ++bx)
           tma_load_3d(sQ + slot * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[slot], bx * C::BOX_ELEMS,
                       qc.it.h, qc.it.q_start + qc.it.r0);
+        ++q_loads;
         qc.next_item(args, n_work);
       };
       while (kc.active && ok) {
@@ -482,6 +485,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                       kc.it.k_start + kc.j * kTileK);
         ++k_it;
         kc.advance(args, n_work);
+      }
+      if (*abort_flag) {  // let this thread's last loads land before the tiles go away
+        for (uint32_t i = 0; i < k_it && i < static_cast<uint32_t>(C::KST); ++i) {
+          const uint32_t n = k_it - 1 - i;
+          if (!mbar_wait_timed(&sm.k_full[n % C::KST], (n / C::KST) & 1, kDrainTimeoutNs)) sm.drain_failed = 1;
+        }
+        for (uint32_t i = 0; i < q_loads && i < static_cast<uint32_t>(C::QST); ++i) {
+          const uint32_t n = q_loads - 1 - i;
+          if (!mbar_wait_timed(&sm.q_full[n % C::QST], (n / C::QST) & 1, kDrainTimeoutNs)) sm.drain_failed = 1;
+        }
       }
     }
   } else if (warp == 3) {
@@ -503,6 +516,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                       vc.it.k_start + vc.j * kTileK);
         ++v_it;
         vc.advance(args, n_work);
+      }
+      if (*abort_flag) {  // let this thread's last loads land before the tiles go away
+        for (uint32_t i = 0; i < v_it && i < static_cast<uint32_t>(C::VST); ++i) {
+          const uint32_t n = v_it - 1 - i;
+          if (!mbar_wait_timed(&sm.v_full[n % C::VST], (n / C::VST) & 1, kDrainTimeoutNs)) sm.drain_failed = 1;
+        }
       }
     }
   } else if (warp == 1) {
@@ -544,6 +563,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ++u;
         sc.advance(args, n_work);
       }
+      if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
+        mma_commit_w(&sm.drain[0]);
+        if (!__all_sync(0xffffffffu, mbar_wait_timed(&sm.drain[0], 0, kDrainTimeoutNs)) && lane == 0)
+          sm.drain_failed = 1;
+      }
     }
   } else if (warp == 2) {
     // ------------------------------------------------ MMA issuer: O += P V (whole warp, one lane issues)
@@ -579,6 +603,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ++u;
         pc.advance(args, n_work);
       }
+      if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
+        mma_commit_w(&sm.drain[1]);
+        if (!__all_sync(0xffffffffu, mbar_wait_timed(&sm.drain[1], 0, kDrainTimeoutNs)) && lane == 0)
+          sm.drain_failed = 1;
+      }
     }
   } else if (warp >= C::ACT_WARP0 && warp < C::ACT_WARP0 + 4 * C::NG) {
     // ------------------------------------------------ activation groups (and epilogue when folded)
@@ -606,16 +635,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto epilogue = [&](const FwdItem& it, float l, float m) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, o_cnt++ & 1, abort_flag))) return false;
       tc_fence_after();
-      float f = v_scale, lse = 0.0f;
-      if (softmax) {  // row sum over the groups' partial sums
-        ssm.stat_l[grp][row] = l;
-        act_groups_sync<C::NG>();
-        float lt = 0.0f;
-#pragma unroll
-        for (int g = 0; g < C::NG; ++g) lt += ssm.stat_l[g][row];
-        f = lt > 0.0f ? v_scale / lt : 0.0f;
-        lse = lt > 0.0f ? m * 0.6931471805599453f + __logf(lt) : -INFINITY;
-      }
+      // softmax runs with two groups and the separate epilogue warps, never here
+      static_assert(!C::SOFTMAX || C::SEP_EPI, "the folded epilogue has no softmax statistics");
+      (void)l;
+      (void)m;
+      const float f = v_scale;
       const int qrow = it.r0 + row;
       const bool row_valid = row < it.rows;
       OutT* orow = out + (static_cast<size_t>(it.q_start + qrow) * pb.h_q + it.h) * C::DV + grp * C::OCOLS;
@@ -662,8 +686,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
       }
-      if (softmax && grp == 0 && row_valid && args.lse != nullptr)
-        args.lse[static_cast<size_t>(it.h) * pb.total_q + it.q_start + qrow] = lse;
       return true;
     };
 
@@ -732,8 +754,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int c0 = col0 + e;
             if (c0 >= c_lo && c0 <= c_hi) mb = fmaxf(mb, __uint_as_float(sa[e]) * s_log2);
           }
+          // exchange through an mbarrier (bounded wait, unlike a named barrier,
+          // so a warp whose wait gave up cannot strand the others here)
           ssm.red[u & 1][grp][row] = mb;
-          act_groups_sync<C::NG>();
+          mbar_arrive(&sm.red_full[u & 1]);
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.red_full[u & 1], (u >> 1) & 1, abort_flag));
+          if (!ok) break;
 #pragma unroll
           for (int g = 0; g < C::NG; ++g) mb = fmaxf(mb, ssm.red[u & 1][g][row]);
           // m is stale by at most 2^8: raise it (and rescale O) only past that
@@ -769,6 +795,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
+#ifdef GDPA_TEST_HOOKS
+        if (!(blockIdx.x == 0 && static_cast<int>(u) == args.test_skip_step))
+#endif
         mbar_arrive(&sm.p_full[b]);
         if (!C::SEP_EPI && j == it.lo && pend) {
           ok = epilogue(pit, pl, pm);
@@ -913,12 +942,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 
   // ------------------------------------------------ teardown
+  // After an abort each role above has waited (time-bounded) for its own
+  // TMA loads and MMAs in flight; only if one of those waits gave up does
+  // the CTA also wait a fixed 1 ms before TMEM and shared memory go away.
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
-    // let copies and MMAs already in flight land before the TMEM and smem go away
-    const unsigned long long t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 1000000ull) {
+    if (sm.drain_failed) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) {
+      }
     }
     if (threadIdx.x == 0) atomicExch(args.status, 5);
   }

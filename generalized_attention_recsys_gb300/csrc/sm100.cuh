@@ -14,7 +14,15 @@
 
 namespace gdpa {
 
+#ifdef GDPA_TEST_HOOKS
+// test-only builds: a wait gives up after 1 ms, so a test can make one run out quickly
+constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull;
+#else
 constexpr unsigned long long kWaitTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s
+#endif
+// Teardown after an abort: how long a role waits for its own copies and
+// MMAs still in flight to land before TMEM and shared memory go away.
+constexpr unsigned long long kDrainTimeoutNs = 1000ull * 1000ull;  // 1 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -87,6 +95,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// Waits for the phase with the given parity for at most timeout_ns, whatever
+// the abort flag says (used on the abort path to let in-flight work land).
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 <= timeout_ns)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 // ---------------------------------------------------------------- proxies / fences

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "../../include/gdpa.h"
@@ -130,7 +131,7 @@ size_t fwd_list_cap(const gdpa_shape* s) {
 size_t bwd_list_cap(const gdpa_shape* s) {
   return static_cast<size_t>(s->total_k) / kTileK + static_cast<size_t>(s->batch) + 1;
 }
-size_t list_bytes(size_t cap) { return round256(16 + 8 * cap); }
+size_t list_bytes(size_t cap) { return round256(offsetof(WorkList, items) + sizeof(WorkEntry) * cap); }
 
 // Deterministic backward: one fp32 dQ slice [total_q, h_q, d_qk] per key block.
 size_t dq_part_bytes(const gdpa_shape* s, int max_k) {
@@ -154,23 +155,27 @@ int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int
   return GDPA_OK;
 }
 
-// Work list: entries (b, blk) sorted by cost, heaviest first (counting sort
-// over cost buckets). mode 0: blk = 128-row query item, cost = KV blocks it
-// visits; mode 1: blk = 128-row key block, cost = query blocks that see it.
+// Work list: one decoded entry (WorkEntry) per block, sorted by cost,
+// heaviest first (counting sort over cost buckets). mode 0: a 128-row query
+// tile, cost = KV blocks it visits; mode 1: a 128-row key block, cost = query
+// blocks that see it.
 constexpr int kBuckets = 2048;
 
-__device__ __forceinline__ int item_cost(const Problem& pb, int mode, int b, int blk, int lq, int lk) {
+// The entry's block fields; w = its number of blocks to visit (the cost).
+__device__ __forceinline__ int4 item_blocks(const Problem& pb, int mode, int blk, int lq, int lk) {
   int lo, hi;
   if (mode == 0) {
     const int r0 = blk * kFwdItemRows;
-    const int r1 = min(lq, r0 + kFwdItemRows) - 1;
-    if (!key_range(r0, r1, lq, lk, pb.causal, pb.window, lo, hi)) return 0;
-    return hi / kTileK - lo / kTileK + 1;
+    const int rows = min(lq - r0, kFwdItemRows);
+    if (rows <= 0 || !key_range(r0, r0 + rows - 1, lq, lk, pb.causal, pb.window, lo, hi))
+      return make_int4(r0, rows > 0 ? rows : 0, 0, 0);
+    return make_int4(r0, rows, lo / kTileK, hi / kTileK - lo / kTileK + 1);
   }
   const int k0 = blk * kTileK;
-  const int k1 = min(lk, k0 + kTileK) - 1;
-  if (!query_range(k0, k1, lq, lk, pb.causal, pb.window, lo, hi)) return 0;
-  return hi / kTileQ - lo / kTileQ + 1;
+  const int krows = min(lk - k0, kTileK);
+  if (krows <= 0 || !query_range(k0, k0 + krows - 1, lq, lk, pb.causal, pb.window, lo, hi))
+    return make_int4(k0, krows > 0 ? krows : 0, 0, 0);
+  return make_int4(k0, krows, lo / kTileQ, hi / kTileQ - lo / kTileQ + 1);
 }
 
 __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, WorkList* wl, int cap) {
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
     const int len = mode == 0 ? lq : lk;
     const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
     for (int blk = 0; blk < nblk; ++blk) {
-      const int c = min(item_cost(pb, mode, b, blk, lq, lk), kBuckets - 1);
+      const int c = min(item_blocks(pb, mode, blk, lq, lk).w, kBuckets - 1);
       atomicAdd(&hist[c], 1);
     }
   }
@@ -231,9 +236,13 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
     const int len = mode == 0 ? lq : lk;
     const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
     for (int blk = 0; blk < nblk; ++blk) {
-      const int c = min(item_cost(pb, mode, b, blk, lq, lk), kBuckets - 1);
+      const int4 bk = item_blocks(pb, mode, blk, lq, lk);
+      const int c = min(bk.w, kBuckets - 1);
       const int p = atomicAdd(&hist[c], 1);
-      if (p < cap) wl->items[p] = make_int2(b, blk);
+      if (p < cap) {
+        wl->items[p].seq = make_int4(qs, lq, ks, lk);
+        wl->items[p].blk = bk;
+      }
     }
   }
 }

@@ -4,9 +4,34 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 
 namespace gdpa {
+
+namespace {
+// Sets a kernel's dynamic shared-memory limit once per device (attributes
+// are per device). Internal linkage on purpose: a static local of a function
+// template would be one object for every loaded copy of this library (the
+// dynamic linker unifies such symbols), so a second copy would skip setting
+// the attribute for its own kernels.
+inline cudaError_t set_smem_limit_once(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(mu);
+  for (const auto& d : done)
+    if (d.first == kern && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(kern, dev);
+  return e;
+}
+}  // namespace
 
 struct FwdArgs {
   Problem pb;

@@ -89,7 +89,7 @@ struct BwdCfg {
 };
 
 struct BwdItem {
-  int b, g, k0, q_start, lq, k_start, lk, krows;
+  int g, k0, q_start, lq, k_start, lk, krows;
   int qlo, nq, nsteps;
 };
 
@@ -98,21 +98,15 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdArgs& a, int pos) {
   const Problem& pb = a.pb;
   const int e = pos / pb.h_kv;
   it.g = pos - e * pb.h_kv;
-  const int2 bb = a.work->items[e];
-  it.b = bb.x;
-  seq_bounds(pb.cu_q, it.b, pb.max_q, it.q_start, it.lq);
-  seq_bounds(pb.cu_k, it.b, pb.max_k, it.k_start, it.lk);
-  it.k0 = bb.y * kTileK;
-  int kr = it.lk - it.k0;
-  it.krows = kr < 0 ? 0 : (kr > kTileK ? kTileK : kr);
-  int rmin, rmax;
-  if (it.krows > 0 && query_range(it.k0, it.k0 + it.krows - 1, it.lq, it.lk, pb.causal, pb.window, rmin, rmax)) {
-    it.qlo = rmin / kTileQ;
-    it.nq = rmax / kTileQ - it.qlo + 1;
-  } else {
-    it.qlo = 0;
-    it.nq = 0;
-  }
+  const int4 sq = a.work->items[e].seq, bk = a.work->items[e].blk;
+  it.q_start = sq.x;
+  it.lq = sq.y;
+  it.k_start = sq.z;
+  it.lk = sq.w;
+  it.k0 = bk.x;
+  it.krows = bk.y;
+  it.qlo = bk.z;
+  it.nq = bk.w;
   it.nsteps = it.nq * pb.group;
   return it;
 }
@@ -797,18 +791,11 @@ cudaError_t launch_bwd_kernel(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               cudaStream_t stream) {
   using C = BwdCfg<DQK, DV, DT, DIRECT>;
   auto kern = gdpa_bwd_kernel<C>;
-  // once per instantiation and device (attributes are per device)
-  static thread_local int attr_dev = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (attr_dev != dev) {
-    // the per-role register split assumes 128 registers a thread at launch
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < 128) return cudaErrorInvalidConfiguration;
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  // the per-role register split assumes 128 registers a thread at launch
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < 128) return cudaErrorInvalidConfiguration;
+  const cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }

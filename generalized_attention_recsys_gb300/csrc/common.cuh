@@ -75,13 +75,27 @@ __host__ __device__ __forceinline__ bool query_range(int k_first, int k_last, in
   return rmax >= rmin;
 }
 
-// Work list written by the schedule kernel: count, then (b, blk) pairs
-// sorted by cost, heaviest first. The kernels visit list position p as
+// One work-list entry, decoded when the list is built, so that a kernel role
+// needs one 32-byte load per item instead of a work-list load followed by
+// dependent cu_seqlens loads:
+//   seq = (q_start, lq, k_start, lk) of the item's sequence;
+//   blk = forward:  (r0, rows, lo, n): the Q tile's first row and row count,
+//                   its first KV block and number of KV blocks (0: no key
+//                   is visible to any of its rows);
+//         backward: (k0, krows, qlo, nq): the key block's first row and row
+//                   count, its first query block and number of query blocks.
+struct WorkEntry {
+  int4 seq;
+  int4 blk;
+};
+
+// Work list written by the schedule kernel: count, then entries sorted by
+// cost, heaviest first. The kernels visit list position p as
 // (entry p / heads, head p % heads).
 struct WorkList {
   int count;
-  int pad[3];
-  int2 items[1];
+  int pad[7];
+  WorkEntry items[1];
 };
 
 // Snake ("zigzag") order over the sorted list: round r visits positions

@@ -118,7 +118,7 @@ struct FwdCfg {
 };
 
 struct FwdItem {
-  int b, h, g, q_start, lq, k_start, lk;
+  int h, g, q_start, lq, k_start, lk;
   int r0, rows, lo, hi, n;
 };
 
@@ -128,23 +128,16 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdArgs& a, int pos) {
   const int e = pos / pb.h_q;
   it.h = pos - e * pb.h_q;
   it.g = it.h / pb.group;
-  const int2 bb = a.work->items[e];
-  it.b = bb.x;
-  seq_bounds(pb.cu_q, it.b, pb.max_q, it.q_start, it.lq);
-  seq_bounds(pb.cu_k, it.b, pb.max_k, it.k_start, it.lk);
-  it.r0 = bb.y * kTileQ;
-  const int rows = it.lq - it.r0;
-  it.rows = rows < 0 ? 0 : (rows > kTileQ ? kTileQ : rows);
-  int kmin, kmax;
-  if (it.rows > 0 && key_range(it.r0, it.r0 + it.rows - 1, it.lq, it.lk, pb.causal, pb.window, kmin, kmax)) {
-    it.lo = kmin / kTileK;
-    it.hi = kmax / kTileK;
-    it.n = it.hi - it.lo + 1;
-  } else {
-    it.lo = 0;
-    it.hi = -1;
-    it.n = 0;
-  }
+  const int4 sq = a.work->items[e].seq, bk = a.work->items[e].blk;
+  it.q_start = sq.x;
+  it.lq = sq.y;
+  it.k_start = sq.z;
+  it.lk = sq.w;
+  it.r0 = bk.x;
+  it.rows = bk.y;
+  it.lo = bk.z;
+  it.n = bk.w;
+  it.hi = it.lo + it.n - 1;
   return it;
 }
 
@@ -345,7 +338,7 @@ __device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint
                                                      const ActConsts& k, int c_lo, int c_hi, const StepSync& sync) {
 #define GDPA_ACT_CASE(A) \
   case A: return act_quarter<C, A, MASKED>(t_s, t_p, col0, k, c_lo, c_hi, sync);
-  if constexpr (C::NG == 4) {
+  if constexpr (C::NG == 4 && C::DT != DT_E4M3) {
     switch (act) {
       GDPA_ACT_CASE(ACT_GELU)
       GDPA_ACT_CASE(ACT_GELU_TANH)
@@ -963,11 +956,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 }
 
+// Whether e4m3 inputs run every elementwise activation with four groups.
+constexpr bool kFp8FourGroups = false;
+
 // Four activation groups where the activation's arithmetic, not the tensor
 // core, sets the pace (16-bit GELU, tanh GELU, SiLU); two elsewhere, which
 // leaves each thread more registers.
 __host__ __device__ constexpr bool fwd_four_groups(int act, int dt) {
-  return dt != DT_E4M3 && (act == ACT_GELU || act == ACT_GELU_TANH || act == ACT_SILU);
+  return dt != DT_E4M3 ? (act == ACT_GELU || act == ACT_GELU_TANH || act == ACT_SILU) : kFp8FourGroups && act != ACT_SOFTMAX;
 }
 
 template <int DQK, int DV, int DT, int NG, bool SOFTMAX = false>
@@ -975,15 +971,8 @@ cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           int grid, cudaStream_t stream) {
   using C = FwdCfg<DQK, DV, DT, NG, SOFTMAX>;
   auto kern = gdpa_fwd_kernel<C>;
-  // once per instantiation and device (the attribute is per device)
-  static thread_local int attr_dev = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (attr_dev != dev) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  const cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
@@ -991,7 +980,7 @@ cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 template <int DQK, int DV, int DT>
 cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                            int grid, cudaStream_t stream) {
-  if constexpr (DT != DT_E4M3) {
+  if constexpr (DT != DT_E4M3 || kFp8FourGroups) {
     if (fwd_four_groups(a.act, DT)) return launch_fwd_ng<DQK, DV, DT, 4>(tq, tk, tv, a, grid, stream);
   }
   if (a.act == ACT_SOFTMAX) return launch_fwd_ng<DQK, DV, DT, 2, true>(tq, tk, tv, a, grid, stream);

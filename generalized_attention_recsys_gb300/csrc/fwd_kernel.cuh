@@ -10,8 +10,8 @@
 // one (sequence, head); its KV blocks form "steps", and all roles walk the
 // same flattened stream of steps across items. Warp roles (128 + 128 NG
 // threads, NG = 2 or 4 activation groups):
-//   warp 0       TMA producer: Q tiles (one item ahead, double-buffered) and
-//                the K ring
+//   warp 0       TMA producers: the K ring (lane 0) and Q tiles (lane 1,
+//                double-buffered, so one item ahead)
 //   warp 1       MMA issuer for S = Q K^T (whole warp; one elected lane issues)
 //   warp 2       MMA issuer for O += P V (likewise)
 //   warp 3       TMA producer: the V ring
@@ -84,6 +84,7 @@ struct FwdCfg {
   static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES;
   // Q double-buffered when two K and two V stages still fit, else single
   static constexpr int QST = AVAIL - 2 * Q_BYTES >= 2 * (K_BYTES + V_BYTES) ? 2 : 1;
+  static_assert(QST <= 4, "at most four Q slots");
   // K needs the deeper ring: S(u) must wait for K(u), whose load can start
   // only once S(u - KST) has released its stage, while V(u) is wanted one
   // GEMM later. Then V takes what is left (at most as many stages as K).
@@ -178,7 +179,7 @@ struct StepCursor {
 };
 
 struct FwdSmem {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[4], q_empty[4];
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
@@ -395,9 +396,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::QST; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], 128 * C::NG);
     }
@@ -437,38 +440,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const uint32_t tbase = sm.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer: Q tiles and the K ring
+    // ------------------------------------------------ TMA producers: the K ring (lane 0) and Q tiles (lane 1)
+    // Separate threads, so that K can run its full ring ahead while a Q slot
+    // is still in use (with one KV block per item, Q slots free only one
+    // item at a time).
     if (lane == 0) {
-      uint32_t k_it = 0, q_loads = 0;
-      StepCursor kc, qc;
+      uint32_t k_it = 0;
+      StepCursor kc;
       kc.start(args, n_work);
-      qc.start(args, n_work);
       bool ok = true;
-      // Q tile of the item under qc into its slot, then move qc on. With
-      // block = false it loads only if the slot is already free, so that a
-      // Q slot still in use does not hold back the K ring.
-      auto load_q = [&](bool block) {
-        const int slot = qc.item_idx % C::QST;
-        const uint32_t par = ((qc.item_idx / C::QST) & 1) ^ 1;
-        if (block) {
-          ok = mbar_wait(&sm.q_empty[slot], par, abort_flag);
-          if (!ok) return;
-        } else if (!mbar_test_wait(&sm.q_empty[slot], par)) {
-          return;
-        }
-        mbar_arrive_expect_tx(&sm.q_full[slot], C::Q_BYTES);
-        for (int bx = 0; bx < C::QK_BOXES; ++bx)
-          tma_load_3d(sQ + slot * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[slot], bx * C::BOX_ELEMS,
-                      qc.it.h, qc.it.q_start + qc.it.r0);
-        ++q_loads;
-        qc.next_item(args, n_work);
-      };
       while (kc.active && ok) {
-        // the Q of the item whose K comes next is on its way first
-        while (ok && qc.active && qc.item_idx <= kc.item_idx) load_q(true);
-        if (!ok) break;
-        // the following item's Q as soon as its slot frees
-        if (qc.active && qc.item_idx == kc.item_idx + 1) load_q(false);
         const int ks = k_it % C::KST;
         ok = mbar_wait(&sm.k_empty[ks], ((k_it / C::KST) & 1) ^ 1, abort_flag);
         if (!ok) break;
@@ -484,6 +465,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t n = k_it - 1 - i;
           if (!mbar_wait_timed(&sm.k_full[n % C::KST], (n / C::KST) & 1, kDrainTimeoutNs)) sm.drain_failed = 1;
         }
+      }
+    } else if (lane == 1) {
+      uint32_t q_loads = 0;
+      StepCursor qc;
+      qc.start(args, n_work);
+      bool ok = true;
+      while (qc.active && ok) {  // one Q tile per item, into the slot that item's predecessors freed
+        const int slot = qc.item_idx % C::QST;
+        ok = mbar_wait(&sm.q_empty[slot], ((qc.item_idx / C::QST) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sm.q_full[slot], C::Q_BYTES);
+        for (int bx = 0; bx < C::QK_BOXES; ++bx)
+          tma_load_3d(sQ + slot * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[slot], bx * C::BOX_ELEMS,
+                      qc.it.h, qc.it.q_start + qc.it.r0);
+        ++q_loads;
+        qc.next_item(args, n_work);
+      }
+      if (*abort_flag) {  // let this thread's last loads land before the tiles go away
         for (uint32_t i = 0; i < q_loads && i < static_cast<uint32_t>(C::QST); ++i) {
           const uint32_t n = q_loads - 1 - i;
           if (!mbar_wait_timed(&sm.q_full[n % C::QST], (n / C::QST) & 1, kDrainTimeoutNs)) sm.drain_failed = 1;

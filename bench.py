@@ -217,21 +217,24 @@ def run_reference(args, wl):
     from generalized_attention_recsys_gb300 import flops, inputs
 
     inp = inputs.make_inputs(wl, seed=args.seed)
-    q, k, v, do = inp.values("q"), inp.values("k"), inp.values("v"), inp.dout.double()
+    q, k, v = inp.values("q"), inp.values("k"), inp.values("v")
+    do = inp.dout.double() if inp.dout is not None else None
     import oracle
 
     units = [(b, h) for b in range(wl.batch) for h in range(wl.h_q)]
     random.Random(args.seed).shuffle(units)
     # a fixed sample per step of about 0.5-1 s of CPU work (two mid-length units)
     step_units = units[:2]
-    fl = sum(3.5 * 2.0 * flops.allowed_pairs([int(inp.lengths_q[b])], [int(inp.lengths_k[b])], wl.causal,
-                                             wl.window) * (wl.d_qk + wl.d_v) for b, _ in step_units)
+    fl = sum((1.0 if do is None else 3.5) * 2.0 *
+             flops.allowed_pairs([int(inp.lengths_q[b])], [int(inp.lengths_k[b])], wl.causal, wl.window) *
+             (wl.d_qk + wl.d_v) for b, _ in step_units)
 
     def step():
         oracle.gdpa_fwd(q, k, v, inp.cu_seqlens_q, inp.cu_seqlens_k, wl.batch, wl.max_q, wl.max_k, wl.act,
                         wl.softmax_scale, wl.causal, wl.window, units=step_units)
-        oracle.gdpa_bwd(q, k, v, do, inp.cu_seqlens_q, inp.cu_seqlens_k, wl.batch, wl.max_q, wl.max_k, wl.act,
-                        wl.softmax_scale, wl.causal, wl.window, units=step_units)
+        if do is not None:
+            oracle.gdpa_bwd(q, k, v, do, inp.cu_seqlens_q, inp.cu_seqlens_k, wl.batch, wl.max_q, wl.max_k, wl.act,
+                            wl.softmax_scale, wl.causal, wl.window, units=step_units)
 
     for _ in range(args.warmup):
         step()
@@ -241,7 +244,8 @@ def run_reference(args, wl):
     dt = time.perf_counter() - t0
     value = fl * args.steps / dt / 1e12
     sample = (f"{len(step_units)} of {len(units)} (sequence, head) units per step (lengths "
-              f"{[int(inp.lengths_q[b]) for b, _ in step_units]}), float64 forward + backward")
+              f"{[int(inp.lengths_q[b]) for b, _ in step_units]}), float64 forward"
+              f"{'' if do is None else ' + backward'}")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
@@ -289,11 +293,18 @@ def main():
 
     inp = inputs.make_inputs(wl, seed=args.seed)
     f_fwd, f_bwd = flops.useful_flops(inp)
+    fwd_only = wl.fwd_only  # forward-only workloads (FP8, and the softmax cross-check at the same shapes)
+    if fwd_only:
+        f_bwd = 0.0
     dev = torch.device("cuda", local_rank)
-    q, k, v, do = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.dout))
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    do = inp.dout.to(dev) if inp.dout is not None else None
     cu_q, cu_k = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
     mq, mk = inp.max_q, inp.max_k
-    out = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=dev)
+    desc = torch.tensor(inp.descale, dtype=torch.float32, device=dev) if inp.descale is not None else None
+    out_dtype = torch.bfloat16 if wl.dtype == "e4m3" else q.dtype
+    out = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=out_dtype, device=dev)
+    lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=dev) if wl.act == "softmax" else None
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     shape = _lib.make_shape(q, k, v, wl.batch)
     ws_f = torch.empty(_lib.gdpa_workspace_bytes(shape, mq, mk, False), dtype=torch.uint8, device=dev)
@@ -301,14 +312,17 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     a = (wl.act, wl.softmax_scale, wl.causal, wl.window)
 
-    def step(qq=q, kk=k, vv=v, dd=do, cq=cu_q, ck=cu_k, ev=None):
+    def step(qq=q, kk=k, vv=v, dd=do, cq=cu_q, ck=cu_k, ev=None, o=None):
+        o = out if o is None else o
         if ev is not None:
             _lib.gdpa_set_profile_events(ev[0], ev[1])
-        _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, out=out, batch=wl.batch, workspace=ws_f)
-        if ev is not None:
-            _lib.gdpa_set_profile_events(ev[2], ev[3])
-        _lib.gdpa_bwd(qq, kk, vv, cq, ck, mq, mk, *a, None, None, dd, dq=dq, dk=dk, dv=dv, batch=wl.batch,
-                      workspace=ws_b)
+        _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, descale_qkv=desc, out=o, lse=lse, batch=wl.batch,
+                      workspace=ws_f)
+        if not fwd_only:
+            if ev is not None:
+                _lib.gdpa_set_profile_events(ev[2], ev[3])
+            _lib.gdpa_bwd(qq, kk, vv, cq, ck, mq, mk, *a, o, lse, dd, dq=dq, dk=dk, dv=dv, batch=wl.batch,
+                          workspace=ws_b)
         if ev is not None:
             _lib.gdpa_set_profile_events(None, None)
 
@@ -346,7 +360,7 @@ def main():
 
     step_ms = sum(s.elapsed_time(e) for s, e in ev_step)
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev_main) / K
-    bwd_ms = sum(e[2].elapsed_time(e[3]) for e in ev_main) / K
+    bwd_ms = sum(e[2].elapsed_time(e[3]) for e in ev_main) / K if not fwd_only else 0.0
     step_ms_max = reduce_max(step_ms, dist, dev)
     value = replica_throughput(f_fwd + f_bwd, K, world, step_ms_max)
 
@@ -356,10 +370,13 @@ def main():
     # buffers are double-buffered. The timed region spans all steps with all of their copies.
     e2e = None
     if not args.no_e2e:
-        host_in = [t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.dout, inp.cu_seqlens_q, inp.cu_seqlens_k)]
+        # inputs q, k, v, (dO), cu_seqlens; results out, (lse), (dq, dk, dv)
+        ins = [inp.q, inp.k, inp.v] + ([inp.dout] if not fwd_only else []) + [inp.cu_seqlens_q, inp.cu_seqlens_k]
+        host_in = [t.pin_memory() for t in ins]
         dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
-        dev_out = [[torch.empty_like(t) for t in (out, dq, dk, dv)] for _ in range(2)]
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, dq, dk, dv)]
+        res = [out] + ([lse] if lse is not None else []) + ([dq, dk, dv] if not fwd_only else [])
+        dev_out = [[torch.empty_like(t) for t in res] for _ in range(2)]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in res]
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         comp = torch.cuda.current_stream()
@@ -379,11 +396,17 @@ def main():
                 in_ready[b].record(s_in)
                 comp.wait_event(in_ready[b])
                 comp.wait_event(out_done[b])  # step i-2's results have left these buffers
-                qq, kk, vv, dd, cq, ck = dev_in[b]
-                o_, dq_, dk_, dv_ = dev_out[b]
-                _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, out=o_, batch=wl.batch, workspace=ws_f)
-                _lib.gdpa_bwd(qq, kk, vv, cq, ck, mq, mk, *a, None, None, dd, dq=dq_, dk=dk_, dv=dv_,
-                              batch=wl.batch, workspace=ws_b)
+                qq, kk, vv = dev_in[b][:3]
+                dd = dev_in[b][3] if not fwd_only else None
+                cq, ck = dev_in[b][-2:]
+                r = dev_out[b]
+                o_, l_ = r[0], (r[1] if lse is not None else None)
+                _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, descale_qkv=desc, out=o_, lse=l_, batch=wl.batch,
+                              workspace=ws_f)
+                if not fwd_only:
+                    dq_, dk_, dv_ = r[-3:]
+                    _lib.gdpa_bwd(qq, kk, vv, cq, ck, mq, mk, *a, o_, l_, dd, dq=dq_, dk=dk_, dv=dv_,
+                                  batch=wl.batch, workspace=ws_b)
                 comp_done[b].record(comp)
                 s_out.wait_event(comp_done[b])
                 with torch.cuda.stream(s_out):
@@ -415,40 +438,62 @@ def main():
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    peak_label = f"{peak_src} bf16 dense (burst)"
+    if wl.dtype == "e4m3":  # the contraction's own dtype: measured bf16 x the nominal e4m3 / bf16 ratio (4.5 / 2.25)
+        peak *= 2.0
+        peak_label = f"{peak_src} bf16 dense (burst) x 2, the nominal e4m3 / bf16 ratio"
     fwd_tflops = f_fwd / (fwd_ms * 1e-3) / 1e12
-    bwd_tflops = f_bwd / (bwd_ms * 1e-3) / 1e12
+    bwd_tflops = f_bwd / (bwd_ms * 1e-3) / 1e12 if not fwd_only else None
     dominant = "gdpa_bwd_kernel" if bwd_ms >= fwd_ms else "gdpa_fwd_kernel"
     dom_flops, dom_ms = (f_bwd, bwd_ms) if dominant == "gdpa_bwd_kernel" else (f_fwd, fwd_ms)
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(dominant, wl.name),
-                "kernel": dominant, "peak_source": f"{peak_src} bf16 dense (burst)",
-                "algorithmic_flops_per_launch": dom_flops, "avg_launch_ms": dom_ms}
+    # algorithmic HBM bytes of one launch: every input read once, every result written once
+    esz = lambda t: t.numel() * t.element_size()  # noqa: E731
+    fwd_bytes = esz(q) + esz(k) + esz(v) + esz(out) + (esz(lse) if lse is not None else 0)
+    bwd_bytes = (esz(q) + esz(k) + esz(v) + (esz(do) if do is not None else 0) + esz(dq) + esz(dk) + esz(dv) +
+                 (esz(out) + esz(lse) if lse is not None else 0))
+    dom_bytes = bwd_bytes if dominant == "gdpa_bwd_kernel" else fwd_bytes
+    hbm = float(peaks["hbm_gbs"])
+    if dom_flops / dom_bytes < peak * 1e12 / (hbm * 1e9):  # below the ridge point: bound by HBM
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": recorded_traffic(dominant, wl.name), "kernel": dominant,
+                    "peak_source": f"{peak_src} HBM copy bandwidth", "algorithmic_bytes_per_launch": dom_bytes,
+                    "avg_launch_ms": dom_ms, "tflops": dom_flops / (dom_ms * 1e-3) / 1e12}
+    else:
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic(dominant, wl.name),
+                    "kernel": dominant, "peak_source": peak_label,
+                    "algorithmic_flops_per_launch": dom_flops, "avg_launch_ms": dom_ms}
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not fwd_only:
         tf, done, total, secs, thr = oracle_sample(inp, args.cpu_seconds, args.seed)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                "sample": f"{done} of {total} (sequence, head) units in seeded random order, float64 forward + "
                          f"backward, {secs:.1f} s"}
 
+    in_mb = (esz(q) + esz(k) + esz(v) + (esz(do) if do is not None else 0)) / 2**20
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name + ": " + wl.notes, "total_tokens": inp.total_q, "max_len": wl.max_q,
                    "seed": args.seed, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
                    "l2": "flushed (256 MB write) before every timed step, outside the step's events; "
-                         "inputs (q,k,v,dO 256 MB) also exceed L2",
+                         f"inputs ({in_mb:.0f} MB) {'also exceed' if in_mb > 129 else 'are within'} L2 (129 MB)",
                    "parallelism": f"replicas x{world}"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
-        "fwd_pct_of_peak": 100.0 * fwd_tflops / peak, "bwd_pct_of_peak": 100.0 * bwd_tflops / peak,
+        "fwd_pct_of_peak": 100.0 * fwd_tflops / peak,
+        "bwd_pct_of_peak": 100.0 * bwd_tflops / peak if bwd_tflops is not None else None,
         "peak_bf16_tflops": {"burst": peak, "sustained": float(peaks.get("bf16_tflops_sustained", 0.0)),
                              "source": peak_src},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 6 * K,
+        # per step: work list + forward kernel; backward: work list, prep, main kernel and (unless dQ
+        # is written directly) the dQ convert
+        "gpu_launches": (2 + (0 if fwd_only else (3 if mk <= 128 else 4))) * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

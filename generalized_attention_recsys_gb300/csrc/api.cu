@@ -155,10 +155,16 @@ int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int
   return GDPA_OK;
 }
 
-// Work list: one decoded entry (WorkEntry) per block, sorted by cost,
-// heaviest first (counting sort over cost buckets). mode 0: a 128-row query
-// tile, cost = KV blocks it visits; mode 1: a 128-row key block, cost = query
-// blocks that see it.
+// Work list: one decoded entry (WorkEntry) per block. mode 0: a 128-row
+// query tile, cost = KV blocks it visits; mode 1: a 128-row key block, cost =
+// query blocks that see it. Sequences are sorted by the cost of their
+// heaviest block, heaviest first (counting sort over cost buckets), and each
+// sequence's blocks stay together in the list, heaviest first (causal: the
+// last query tile / the first key block). Zigzag dealing then gives every CTA
+// a balanced mix, and the blocks that share a sequence's K and V (or, in the
+// backward, its Q, dO and dQ rows) run at the same time on neighbouring
+// CTAs, so those tiles are read from DRAM about once rather than once per
+// block when the problem outgrows L2.
 constexpr int kBuckets = 2048;
 
 // The entry's block fields; w = its number of blocks to visit (the cost).
@@ -178,6 +184,13 @@ __device__ __forceinline__ int4 item_blocks(const Problem& pb, int mode, int blk
   return make_int4(k0, krows, lo / kTileQ, hi / kTileQ - lo / kTileQ + 1);
 }
 
+// Cost bucket of a sequence: its heaviest block's cost.
+__device__ __forceinline__ int seq_bucket(const Problem& pb, int mode, int nblk, int lq, int lk) {
+  int c = 0;
+  for (int blk = 0; blk < nblk; ++blk) c = max(c, item_blocks(pb, mode, blk, lq, lk).w);
+  return min(c, kBuckets - 1);
+}
+
 __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, WorkList* wl, int cap) {
   __shared__ int hist[kBuckets];
   for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
@@ -189,10 +202,7 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
     seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
     const int len = mode == 0 ? lq : lk;
     const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
-    for (int blk = 0; blk < nblk; ++blk) {
-      const int c = min(item_blocks(pb, mode, blk, lq, lk).w, kBuckets - 1);
-      atomicAdd(&hist[c], 1);
-    }
+    if (nblk > 0) atomicAdd(&hist[seq_bucket(pb, mode, nblk, lq, lk)], nblk);
   }
   __syncthreads();
   // exclusive prefix over the buckets, heaviest first: each of the 1024
@@ -235,13 +245,15 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
     seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
     const int len = mode == 0 ? lq : lk;
     const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
-    for (int blk = 0; blk < nblk; ++blk) {
-      const int4 bk = item_blocks(pb, mode, blk, lq, lk);
-      const int c = min(bk.w, kBuckets - 1);
-      const int p = atomicAdd(&hist[c], 1);
+    if (nblk == 0) continue;
+    const int base = atomicAdd(&hist[seq_bucket(pb, mode, nblk, lq, lk)], nblk);  // the sequence's slots
+    for (int i = 0; i < nblk; ++i) {
+      // causal costs grow with the query tile and shrink with the key block: heaviest first
+      const int blk = mode == 0 ? nblk - 1 - i : i;
+      const int p = base + i;
       if (p < cap) {
         wl->items[p].seq = make_int4(qs, lq, ks, lk);
-        wl->items[p].blk = bk;
+        wl->items[p].blk = item_blocks(pb, mode, blk, lq, lk);
       }
     }
   }

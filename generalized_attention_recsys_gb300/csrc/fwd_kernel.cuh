@@ -267,6 +267,38 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
   }
 }
 
+// Bit e set when column cb + e (0 <= e < 32) lies in [lo, hi].
+__device__ __forceinline__ uint32_t cols_in_range(int cb, int lo, int hi) {
+  const int a = max(lo - cb, 0), b = min(hi - cb, 31);
+  if (a > b) return 0u;
+  return (0xFFFFFFFFu >> (31 - b)) & (0xFFFFFFFFu << a);
+}
+
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Zeroes the masked elements of 32 packed P values (bit e of m: column e
+// kept). Bits 4i..4i+3 are moved to the top bit of bytes 0..3 by one multiply
+// (the four shifted copies of the nibble do not overlap), and prmt's
+// sign-replicating selectors widen each top bit to its byte (e4m3: one column
+// per byte) or to both bytes of its half-word (bf16 / f16 pairs).
+template <int DT>
+__device__ __forceinline__ void mask_p_words(uint32_t (&w)[16], uint32_t m) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t y = ((m >> (4 * i)) & 0xFu) * 0x10204080u;
+    if constexpr (DT == DT_E4M3) {
+      w[i] &= prmt_b32(y, y, 0xBA98u);
+    } else {
+      w[2 * i] &= prmt_b32(y, y, 0x9988u);
+      w[2 * i + 1] &= prmt_b32(y, y, 0xBBAAu);
+    }
+  }
+}
+
 // P = where(c_lo <= col <= c_hi, act(scale * S), 0) for one group's GCOLS
 // columns of an S tile, 32 at a time; thread = one row (TMEM lane). t_s /
 // t_p: this lane's address of the group's first S / P column.
@@ -283,28 +315,14 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
     const uint32_t(&sa)[32] = sv[ch];
     uint32_t pk[16];
     if constexpr (ACT == ACT_FAST_GELU_BF16 && C::DT == DT_BF16) {
-      // already bf16 pairs: store them as they come, masking by halves
+      // already bf16 pairs: stored as they come
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        uint32_t w = fast_gelu_bf16_pair(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1]), k);
-        if (MASKED) {
-          const int c = col0 + 32 * ch + 2 * e;
-          w &= ((c >= c_lo && c <= c_hi) ? 0x0000FFFFu : 0u) | ((c + 1 >= c_lo && c + 1 <= c_hi) ? 0xFFFF0000u : 0u);
-        }
-        pk[e] = w;
-      }
+      for (int e = 0; e < 16; ++e) pk[e] = fast_gelu_bf16_pair(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1]), k);
     } else if constexpr (ACT == ACT_GELU && C::DT == DT_BF16) {
       // mixed tanh form / polynomial, packed by truncation (constants carry the bias)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        uint32_t w =
-            pack_trunc_bf16x2(gelu_mixed_pair<true>(e, f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1])), k));
-        if (MASKED) {
-          const int c = col0 + 32 * ch + 2 * e;
-          w &= ((c >= c_lo && c <= c_hi) ? 0x0000FFFFu : 0u) | ((c + 1 >= c_lo && c + 1 <= c_hi) ? 0xFFFF0000u : 0u);
-        }
-        pk[e] = w;
-      }
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_trunc_bf16x2(gelu_mixed_pair<true>(e, f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1])), k));
     } else {
     float p[32];
 #pragma unroll
@@ -313,17 +331,12 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
       f2_t r;
       if constexpr (ACT == ACT_GELU) r = gelu_mixed_pair<false>(e, sp, k);
       else r = act_pair<ACT>(sp, k);
-      float v0 = f2_lo(r), v1 = f2_hi(r);
-      if (MASKED) {
-        const int c = col0 + 32 * ch + 2 * e;
-        v0 = (c >= c_lo && c <= c_hi) ? v0 : 0.0f;
-        v1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? v1 : 0.0f;
-      }
-      p[2 * e] = v0;
-      p[2 * e + 1] = v1;
+      p[2 * e] = f2_lo(r);
+      p[2 * e + 1] = f2_hi(r);
     }
     pack_p_chunk<C::DT>(p, pk);
     }
+    if (MASKED) mask_p_words<C::DT>(pk, cols_in_range(col0 + 32 * ch, c_lo, c_hi));
     if (ch == 0 && !sync.wait_p_buffer()) return false;  // first store into the buffer
     store_p_chunk<C::DT>(t_p + ch * C::P_COLS_PER_32, pk);
   }

@@ -330,6 +330,9 @@ __device__ __forceinline__ bool act_quarter(uint32_t t_s, uint32_t t_p, int col0
       const f2_t sp = f2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1]));
       f2_t r;
       if constexpr (ACT == ACT_GELU) r = gelu_mixed_pair<false>(e, sp, k);
+      else if constexpr (C::DT == DT_E4M3 && (ACT == ACT_FAST_GELU || ACT == ACT_GELU_TANH))
+        r = fast_gelu_mixed_pair(e, sp, k);
+      else if constexpr (C::DT == DT_E4M3 && ACT == ACT_SILU) r = act_pair<ACT_FAST_SILU>(sp, k);
       else r = act_pair<ACT>(sp, k);
       p[2 * e] = f2_lo(r);
       p[2 * e + 1] = f2_hi(r);

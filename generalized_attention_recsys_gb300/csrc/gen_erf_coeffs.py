@@ -16,6 +16,11 @@ and MUFU pipes share the work (act.cuh):
 
 The report gives each fit's max |Phi error| in float64.
 
+FastGELU forward with e4m3 P: its own tanh factor fitted the same way as
+the erf polynomial: tanh(sqrt(2/pi) (z + 0.044715 z^3)) ~ v t(v^2) with
+v = z / Z clamped to [-1, 1], t of degree 5, Z scanned, minimax over
+z in [0, 10] with the clamp applied (|Phi error| is half the tanh error).
+
 Backward (MUFU rcp + ex2): for x >= 0 the form of Abramowitz & Stegun,
 Handbook of Mathematical Functions, 7.1.25 (Hastings' approximation):
 
@@ -68,6 +73,32 @@ def best_poly(n: int) -> tuple[float, np.ndarray, float]:
         if best is None or e < best[2]:
             best = (float(xc), c, e)
     c, e = fit_poly(best[0], n)
+    return best[0], c, e
+
+
+def fit_fast_gelu_poly(z_clamp: float, n: int, iters: int = 300) -> tuple[np.ndarray, float]:
+    """tanh(u(z)) ~ v t(v^2), v = min(z / z_clamp, 1), minimax over z in [0, 10]; returns (t, max |tanh error|)."""
+    z = np.linspace(0.0, 10.0, 40001)
+    y = np.tanh(np.sqrt(2.0 / np.pi) * (z + 0.044715 * z ** 3))
+    v = np.minimum(z / z_clamp, 1.0)
+    u = v * v
+    basis = np.stack([v * u ** i for i in range(n)], axis=1)
+    w = np.ones_like(z)
+    for _ in range(iters):
+        c, *_ = np.linalg.lstsq(basis * np.sqrt(w)[:, None], y * np.sqrt(w), rcond=None)
+        err = np.abs(basis @ c - y)
+        w = w * (err / err.max() + 1e-4)
+        w /= w.mean()
+    return c, float(np.abs(basis @ c - y).max())
+
+
+def best_fast_gelu_poly(n: int) -> tuple[float, np.ndarray, float]:
+    best = None
+    for zc in np.arange(2.8, 4.2, 0.05):
+        c, e = fit_fast_gelu_poly(float(zc), n, 150)
+        if best is None or e < best[2]:
+            best = (float(zc), c, e)
+    c, e = fit_fast_gelu_poly(best[0], n)
     return best[0], c, e
 
 
@@ -142,6 +173,12 @@ if __name__ == "__main__":
     for i, ci in enumerate(cp):
         print(f"//   p[{i}] = {float(np.float32(ci))!r}f")
     ct, et = fit_tanh_form()
+    zc, cf, ef = best_fast_gelu_poly(POLY_TERMS)
+    print(f"// FastGELU tanh factor ~ v t(v^2), v = clamp(z / {zc:.2f}, -1, 1): max |tanh error| {ef:.2e}, "
+          f"|Phi error| {ef / 2:.2e}")
+    print(f"constexpr float kFastGeluPolyZ = {float(np.float32(zc))!r}f;")
+    for i, ci in enumerate(cf):
+        print(f"//   t[{i}] = {float(np.float32(ci))!r}f")
     print(f"// Phi(z) ~ (1 + tanh(a z + b z^3)) / 2: max |Phi error| {et:.2e}")
     print(f"constexpr float kPhiTanhA = {float(np.float32(ct[0]))!r}f;")
     print(f"constexpr float kPhiTanhB = {float(np.float32(ct[1]))!r}f;")

@@ -84,3 +84,54 @@ def test_device_activation_and_derivative_pointwise(act):
                              f"got {got_f[rows[:5], cols[:5]].tolist()} ref {ref_f[rows[:5], cols[:5]].tolist()}")
     assert not bad_g.any(), f"{act}: act' mismatch at z={zz[bad_g][:5].tolist()} got {got_g[bad_g][:5].tolist()} " \
                             f"ref {ref_g[bad_g][:5].tolist()}"
+
+
+# e4m3 forward: bound of the device evaluation before P is rounded to e4m3,
+# as a multiple of max(1, |z|). gelu as for 16-bit P; fast_gelu and gelu_tanh
+# mix the MUFU tanh form (about 2^-11 of tanh) with a fitted polynomial
+# (|Phi error| <= 1.6e-4); silu takes fast_silu's MUFU tanh form.
+FP8_BOUND = {"gelu": 4e-4, "gelu_tanh": 6e-4, "fast_gelu": 6e-4, "silu": 6e-4, "fast_silu": 6e-4,
+             "fast_gelu_bf16": 6e-3}
+
+
+@pytest.mark.parametrize("act", ELEMENTWISE)
+def test_device_activation_pointwise_e4m3(act):
+    # z = a + b / 32 with a, b e4m3 codes (exact in the fp32 accumulator);
+    # every key is (1, 1/32, 0, ...) and v the identity, so out[i, j] is the
+    # kernel's e4m3 P at tile column j, exactly representable in bf16.
+    ensure_built()
+    codes = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    a = codes[torch.isfinite(codes) & (codes.abs() <= 9)]
+    b = torch.arange(-16.0, 17.0)
+    z = (a[:, None] + b[None, :] / 32).reshape(-1)
+    z, idx = torch.unique(z, return_inverse=True, sorted=True)
+    aa = (a[:, None] + 0 * b[None, :]).reshape(-1)
+    bb = (0 * a[:, None] + b[None, :]).reshape(-1)
+    rep = torch.empty(z.numel(), dtype=torch.long).scatter_(0, idx, torch.arange(idx.numel()))  # one (a, b) per z
+    n, d, nk = z.numel(), 128, 128
+    q = torch.zeros(n, 1, d)
+    q[:, 0, 0] = aa[rep]
+    q[:, 0, 1] = bb[rep]
+    kf = torch.zeros(nk, 1, d)
+    kf[:, 0, 0] = 1
+    kf[:, 0, 1] = 1.0 / 32
+    vf = torch.eye(nk, d).reshape(nk, 1, d)
+    f8 = torch.float8_e4m3fn
+    assert torch.equal(q.to(f8).float(), q) and torch.equal(kf.to(f8).float(), kf)
+    cu_q = torch.tensor([0, n], dtype=torch.int32).cuda()
+    cu_k = torch.tensor([0, nk], dtype=torch.int32).cuda()
+    desc = torch.ones(3, dtype=torch.float32).cuda()
+    out, _ = _lib.gdpa_fwd(q.to(f8).cuda(), kf.to(f8).cuda(), vf.to(f8).cuda(), cu_q, cu_k, n, nk, act, 1.0,
+                           descale_qkv=desc, batch=1)
+    assert _lib.gdpa_get_status() == 0
+    zz = z.double()
+    assert torch.equal(q[:, 0, 0].double() + q[:, 0, 1].double() / 32, zz)
+    ref = oracle.act_fwd(act, zz)[:, None].expand(n, nk)
+    got = out[:, 0, :nk].double().cpu()
+    # half an e4m3 ulp: 2^-4 of the value (normal), 2^-10 (subnormal step 2^-9)
+    bound = 2.0 ** -4 * ref.abs() + 2.0 ** -10 + 1.07 * FP8_BOUND.get(act, 2e-5) * torch.clamp(zz.abs(), min=1.0)[:, None]
+    bad = (got - ref).abs() > bound
+    if bad.any():
+        rows, cols = torch.nonzero(bad, as_tuple=True)
+        raise AssertionError(f"{act}: e4m3 P mismatch at z={zz[rows[:5]].tolist()} columns {cols[:5].tolist()} "
+                             f"got {got[rows[:5], cols[:5]].tolist()} ref {ref[rows[:5], cols[:5]].tolist()}")

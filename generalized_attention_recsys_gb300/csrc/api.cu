@@ -368,7 +368,6 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   int st = validate(s, max_q, max_k, act, causal, window);
   if (st != GDPA_OK) return st;
   if (s->dtype == GDPA_E4M3) return GDPA_ERR_UNSUPPORTED;
-  if (s->d_qk > 128) return GDPA_ERR_UNSUPPORTED;  // (192,128) backward: TMEM plan holds dims <= 128
   if (s->batch == 0 || (s->total_q == 0 && s->total_k == 0)) return GDPA_OK;
   if ((cu_q == nullptr) != (cu_k == nullptr)) return GDPA_ERR_INVALID;
   if (!cu_q && (s->total_q != s->batch * max_q || s->total_k != s->batch * max_k)) return GDPA_ERR_INVALID;

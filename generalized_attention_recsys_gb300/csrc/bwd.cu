@@ -17,7 +17,10 @@ cudaError_t launch_bwd_d96(int dtype, const CUtensorMap& tq, const CUtensorMap& 
                            cudaStream_t stream);
 cudaError_t launch_bwd_d128(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
-                           cudaStream_t stream);
+                            cudaStream_t stream);
+cudaError_t launch_bwd_d192(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                            cudaStream_t stream);
 
 namespace {
 
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Probl
     seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
     seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
     const int qb = (t - qs) / kTileQ;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // columns lane, lane + 32, ... (d <= 128)
+    float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // columns lane, lane + 32, ... (d <= 192)
     // the workspace holds n_slices; a longer key sequence (max_k understated)
     // was reported by the main kernel, which wrote no slice beyond them
     const int nkv = min(lk > 0 ? (lk + kTileK - 1) / kTileK : 0, n_slices);
@@ -139,11 +142,11 @@ __global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Probl
       if (qb < rmin / kTileQ || qb > rmax / kTileQ) continue;
       const float* src = part + (static_cast<size_t>(j) * pb.total_q * pb.h_q + r) * d;
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
+      for (int m = 0; m < 6; ++m)
         if (lane + 32 * m < d) acc[m] += src[lane + 32 * m];
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+    for (int m = 0; m < 6; ++m)
       if (lane + 32 * m < d) dq[r * d + lane + 32 * m] = from_f<T>(acc[m]);
   }
 }
@@ -182,6 +185,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     case 64: e = launch_bwd_d64(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
     case 96: e = launch_bwd_d96(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
     case 128: e = launch_bwd_d128(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
+    case 192: e = launch_bwd_d192(a.dtype, tq, tk, tv, tdo, tdq, a, grid, stream); break;
     default: return cudaErrorNotSupported;
   }
   if (e != cudaSuccess) return e;

@@ -24,6 +24,15 @@
 // TMEM (512 columns): S^T [0,128) with P^T written over it, dP^T [128,256)
 // reused for dQ once dP^T has been read, dV [256,256+dv), dK [384,384+dqk).
 //
+// d_qk = 192 (with d_v = 128): 192-column dK and dQ accumulators do not fit
+// beside S^T, dP^T and dV, so dK and dQ are computed in column parts, [0,128)
+// and [128,192), each part its own work item: both recompute S^T, P^T, dP^T
+// and dS^T (the activation and its derivative), part 0 also computes dV. The
+// two parts of a key block are neighbours in the work order, so they run at
+// the same time on two CTAs and read K, V, Q and dO from L2 once. Shared
+// memory then holds one Q stage: the next Q tile loads after dK has read the
+// current one, and each step issues dQ and dK before the next S^T.
+//
 // Warp roles (128 * (NG + 2) threads): warp 0 TMA for K/V, warp 1 MMA,
 // warp 2 TMA for Q, warp 3 TMA for dO, NG elementwise groups of four warps
 // (128 / NG query columns of each tile each), then four warps that drain dQ
@@ -53,7 +62,12 @@ struct BwdCfg {
   static constexpr int DQK = DQK_, DV = DV_, DT = DT_;
   static constexpr bool DIRECT_DQ = DIRECT_DQ_;
   static_assert(DT == DT_BF16 || DT == DT_FP16, "backward takes 16-bit inputs");
-  static_assert(DQK <= 128 && DV <= 128, "backward TMEM plan holds head dims up to 128");
+  static_assert((DQK <= 128 && DV <= 128) || (DQK == 192 && DV == 128), "backward head dims up to 128, or (192, 128)");
+  // dK / dQ column parts: [0, PART_COLS0) and, for d_qk = 192, [128, 192)
+  static constexpr int NPART = DQK > 128 ? 2 : 1;
+  static constexpr int PART_COLS0 = DQK > 128 ? 128 : DQK;
+  static constexpr int PART_COLS1 = DQK - PART_COLS0;
+  static constexpr int PART_NCH_MAX = PART_COLS0 / 32;  // 32-column chunks of the wider part
   static constexpr int BOX_ELEMS = 64;
   static constexpr int BOX_BYTES = 128 * 128;
   static constexpr int QK_BOXES = (DQK + 63) / 64;
@@ -63,7 +77,8 @@ struct BwdCfg {
   static constexpr int Q_BYTES = K_BYTES;
   static constexpr int DO_BYTES = V_BYTES;
   static constexpr int DS_BYTES = 2 * BOX_BYTES;
-  static constexpr int Q_STAGES = 2;  // dO is single-buffered: its next tile loads while S^T, dQ, dK run
+  // dO is single-buffered: its next tile loads while S^T, dQ, dK run
+  static constexpr int Q_STAGES = DQK > 128 ? 1 : 2;
   static constexpr int DQ_CHUNK_BYTES = 32 * 128;              // 32 query rows x 32 fp32 columns
   static constexpr int DQ_STAGE_BYTES = 4 * 2 * DQ_CHUNK_BYTES;  // per drain warp: a ring of two chunks
   static constexpr int BAR_BYTES = 512;
@@ -77,8 +92,10 @@ struct BwdCfg {
   static constexpr uint32_t FMT = DT == DT_BF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_S = idesc_make(128, 128, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_DV = idesc_make(128, DV, FMT, FMT, 0, 1);
-  static constexpr uint32_t IDESC_DK = idesc_make(128, DQK, FMT, FMT, 0, 1);
-  static constexpr uint32_t IDESC_DQ = idesc_make(128, DQK, FMT, FMT, 1, 1);
+  static constexpr uint32_t IDESC_DK0 = idesc_make(128, PART_COLS0, FMT, FMT, 0, 1);
+  static constexpr uint32_t IDESC_DQ0 = idesc_make(128, PART_COLS0, FMT, FMT, 1, 1);
+  static constexpr uint32_t IDESC_DK1 = idesc_make(128, NPART > 1 ? PART_COLS1 : PART_COLS0, FMT, FMT, 0, 1);
+  static constexpr uint32_t IDESC_DQ1 = idesc_make(128, NPART > 1 ? PART_COLS1 : PART_COLS0, FMT, FMT, 1, 1);
   static constexpr int NG = 2;             // elementwise groups (4 warps each), 64 query columns each
   static constexpr int GCOLS = kTileQ / NG;  // query columns per group
   static constexpr int GCHUNKS = GCOLS / 16;
@@ -89,15 +106,19 @@ struct BwdCfg {
 };
 
 struct BwdItem {
-  int g, k0, q_start, lq, k_start, lk, krows;
+  int g, part, k0, q_start, lq, k_start, lk, krows;
   int qlo, nq, nsteps;
 };
 
-__device__ __forceinline__ BwdItem bwd_decode(const BwdArgs& a, int pos) {
+// Item pos: work-list entry pos / (h_kv npart), then its column part, then the kv head.
+__device__ __forceinline__ BwdItem bwd_decode(const BwdArgs& a, int pos, int npart) {
   BwdItem it;
   const Problem& pb = a.pb;
-  const int e = pos / pb.h_kv;
-  it.g = pos - e * pb.h_kv;
+  const int per = pb.h_kv * npart;
+  const int e = pos / per;
+  const int r = pos - e * per;
+  it.part = npart > 1 ? r / pb.h_kv : 0;
+  it.g = r - it.part * pb.h_kv;
   const int4 sq = a.work->items[e].seq, bk = a.work->items[e].blk;
   it.q_start = sq.x;
   it.lq = sq.y;
@@ -109,6 +130,12 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdArgs& a, int pos) {
   it.nq = bk.w;
   it.nsteps = it.nq * pb.group;
   return it;
+}
+
+// The item's column part, a compile-time 0 when there is only one.
+template <class C>
+__device__ __forceinline__ int item_part(const BwdItem& it) {
+  return C::NPART > 1 ? it.part : 0;
 }
 
 // Query head and first row of step s of an item.
@@ -290,7 +317,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const Problem& pb = args.pb;
-  const int n_work = args.work->count * pb.h_kv;
+  const int n_work = args.work->count * pb.h_kv * C::NPART;
   const int G = gridDim.x;
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -349,7 +376,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int round = 0; ok; ++round) {
         const int pos = zigzag_pos(round, blockIdx.x, G);
         if (pos >= n_work) break;
-        const BwdItem it = bwd_decode(args, pos);
+        const BwdItem it = bwd_decode(args, pos, C::NPART);
         if (it.nsteps == 0) continue;
         if (warp == 0) {
           ok = mbar_wait(&sm.kv_empty, (kv_cnt++ & 1) ^ 1, abort_flag);
@@ -429,17 +456,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           mma_f16_ts_w(tbase + C::T_DV, tbase + C::T_S + pt_col<C>(k), sdesc_at(dDO_mn, k * 2048), C::IDESC_DV,
                        (acc || k > 0) ? 1u : 0u);
       };
-      auto issue_dq = [&]() {  // dQ = dS K
+      // dQ and dK of column part `part` (columns from 128 part: 64-column boxes 2 part on)
+      auto issue_dq = [&](int part) {  // dQ = dS K
+        const uint32_t boff = part * 2 * C::BOX_BYTES;
+        const uint32_t idesc = part ? C::IDESC_DQ1 : C::IDESC_DQ0;
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k)
-          mma_f16_ss_w(tbase + C::T_DQ, sdesc_at(dDS_mn, k * 2048), sdesc_at(dK_mn, k * 2048), C::IDESC_DQ, k > 0);
+          mma_f16_ss_w(tbase + C::T_DQ, sdesc_at(dDS_mn, k * 2048), sdesc_at(dK_mn, boff + k * 2048), idesc, k > 0);
         mma_commit_w(&sm.dq_full);
       };
-      auto issue_dk = [&](int st, bool acc) {  // dK += dS^T Q
+      auto issue_dk = [&](int st, bool acc, int part) {  // dK += dS^T Q
+        const uint32_t boff = part * 2 * C::BOX_BYTES;
+        const uint32_t idesc = part ? C::IDESC_DK1 : C::IDESC_DK0;
 #pragma unroll
         for (int k = 0; k < C::T_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
-          mma_f16_ss_w(tbase + C::T_DK, sdesc_at(dDS_k, off), sdesc_at(dQ_mn, st * C::Q_BYTES + k * 2048), C::IDESC_DK,
+          mma_f16_ss_w(tbase + C::T_DK, sdesc_at(dDS_k, off), sdesc_at(dQ_mn, st * C::Q_BYTES + boff + k * 2048), idesc,
                        (acc || k > 0) ? 1u : 0u);
         }
       };
@@ -453,6 +485,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // and pass 2(t) has finished; dQ's drain overlaps dK, before dP^T(t+1)
       // reuses the dQ columns; the commit after dP^T(t+1) also covers dQ(t)
       // and dK(t), so pass 2(t+1) may overwrite the dS tile they read.
+      // With one Q stage, Q(t+1) loads only once dK(t) has read Q(t), so the
+      // order is dK(t), dQ(t), S^T(t+1), dP^T(t+1), dV(t+1). Column part 1
+      // (d_qk = 192) computes no dV: dP^T is then its dO tile's last reader.
       const bool s_first = bwd_s_first(args.act);
       uint32_t kv_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, dqe = 0, acce = 0;
       bool ok = true;
@@ -468,50 +503,64 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mma_commit_w(&sm.s_full);
         return true;
       };
-      auto issue_dp_dv_at = [&](uint32_t it_idx, bool first) -> bool {
+      auto issue_dp_dv_at = [&](uint32_t it_idx, bool first, int part) -> bool {
         if (!wait_all(&sm.dq_empty, (dqe++ & 1) ^ 1)) return false;
         if (!wait_all(&sm.do_full, it_idx & 1)) return false;
         tc_fence_after();
         issue_dp();
         mma_commit_w(&sm.dp_full);
+        if (part != 0) mma_commit_w(&sm.do_empty);  // no dV: dP^T is the last reader of this dO tile
         if (!wait_all(&sm.p_full, p_cnt++ & 1)) return false;
+        // the previous item's dV / dK epilogue has read TMEM before this item's first dV / dK
         if (first && !wait_all(&sm.acc_empty, (acce++ & 1) ^ 1)) return false;
-        tc_fence_after();
-        issue_dv(!first);
-        mma_commit_w(&sm.do_empty);  // dV is the last reader of this dO tile
+        if (part == 0) {
+          tc_fence_after();
+          issue_dv(!first);
+          mma_commit_w(&sm.do_empty);  // dV is the last reader of this dO tile
+        }
         return true;
       };
       for (int round = 0; ok; ++round) {
         const int pos = zigzag_pos(round, blockIdx.x, G);
         if (pos >= n_work) break;
-        const BwdItem it = bwd_decode(args, pos);
+        const BwdItem it = bwd_decode(args, pos, C::NPART);
         if (it.nsteps == 0) continue;
         ok = wait_all(&sm.kv_full, kv_cnt++ & 1);
         if (ok) ok = issue_s_at(qd_it);
-        if (ok) ok = issue_dp_dv_at(qd_it, true);
+        if (ok) ok = issue_dp_dv_at(qd_it, true, item_part<C>(it));
         for (int s = 0; s < it.nsteps && ok; ++s) {
           const int st = qd_it % C::Q_STAGES;
           const bool more = s + 1 < it.nsteps;
           ok = wait_all(&sm.ds_full, ds_cnt++ & 1);
           if (!ok) break;
-          if (s_first && more && !issue_s_at(qd_it + 1)) {
+          if (C::Q_STAGES > 1 && s_first && more && !issue_s_at(qd_it + 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_dq();
-          if (!s_first && more && !issue_s_at(qd_it + 1)) {
+          if (C::Q_STAGES == 1) {  // dK first: the next Q tile loads while dQ runs
+            issue_dk(st, s > 0, item_part<C>(it));
+            mma_commit_w(&sm.q_empty[st]);
+          }
+          issue_dq(item_part<C>(it));
+          if (C::Q_STAGES > 1 && !s_first && more && !issue_s_at(qd_it + 1)) {
             ok = false;
             break;
           }
-          issue_dk(st, s > 0);
-          mma_commit_w(&sm.q_empty[st]);
+          if (C::Q_STAGES > 1) {
+            issue_dk(st, s > 0, item_part<C>(it));
+            mma_commit_w(&sm.q_empty[st]);
+          }
+          if (C::Q_STAGES == 1 && more && !issue_s_at(qd_it + 1)) {
+            ok = false;
+            break;
+          }
           ++qd_it;
           if (!more) {
             mma_commit_w(&sm.acc_full);
             mma_commit_w(&sm.kv_empty);
           } else {
-            ok = issue_dp_dv_at(qd_it, false);
+            ok = issue_dp_dv_at(qd_it, false, item_part<C>(it));
           }
         }
       }
@@ -536,18 +585,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int round = 0; ok; ++round) {
       const int pos = zigzag_pos(round, blockIdx.x, G);
       if (pos >= n_work) break;
-      const BwdItem it = bwd_decode(args, pos);
+      const BwdItem it = bwd_decode(args, pos, C::NPART);
       const int kk = it.k0 + row;
       const bool row_valid = row < it.krows;
-      // the epilogue splits the 32-column chunks of dV then dK round-robin over the groups
+      // the epilogue splits the 32-column chunks of dV (column part 0 only)
+      // then of this part's dK columns round-robin over the groups
       const size_t krow = static_cast<size_t>(it.k_start + kk) * pb.h_kv + it.g;
       T* dv_row = reinterpret_cast<T*>(args.dv) + krow * C::DV;
-      T* dk_row = reinterpret_cast<T*>(args.dk) + krow * C::DQK;
-      constexpr int NCH = (C::DV + C::DQK) / 32;
+      T* dk_row = reinterpret_cast<T*>(args.dk) + krow * C::DQK + item_part<C>(it) * 128;
+      const int n_dv = item_part<C>(it) == 0 ? C::DV / 32 : 0;
+      const int nch = n_dv + (item_part<C>(it) == 0 ? C::PART_COLS0 : C::PART_COLS1) / 32;
       if (it.nsteps == 0) {
         if (row_valid)
-          for (int ch = w; ch < NCH; ch += C::NG) {
-            T* d = ch < C::DV / 32 ? dv_row + ch * 32 : dk_row + (ch - C::DV / 32) * 32;
+          for (int ch = w; ch < nch; ch += C::NG) {
+            T* d = ch < n_dv ? dv_row + ch * 32 : dk_row + (ch - n_dv) * 32;
             for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(d)[q4] = make_uint4(0, 0, 0, 0);
           }
         continue;
@@ -594,9 +645,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int ch = w; ch < NCH; ch += C::NG) {
-        const bool is_dv = ch < C::DV / 32;
-        const int cc = is_dv ? ch * 32 : (ch - C::DV / 32) * 32;
+      for (int ch = w; ch < nch; ch += C::NG) {
+        const bool is_dv = ch < n_dv;
+        const int cc = is_dv ? ch * 32 : (ch - n_dv) * 32;
         uint32_t o[32];
         tmem_ld32(t_lane + (is_dv ? C::T_DV : C::T_DK) + cc, o);
         tmem_ld_wait(o);
@@ -625,13 +676,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int row = quad * 32 + lane;  // query row within the tile
     const uint32_t t_dq = tbase + (static_cast<uint32_t>(quad * 32) << 16) + C::T_DQ;
     uint8_t* stage_base = sDQ + quad * 2 * C::DQ_CHUNK_BYTES;  // this warp's two 32 x 32 fp32 boxes
-    constexpr int NCH = C::DQK / 32, NPAIR = (NCH + 1) / 2;
+    constexpr int NPAIR_MAX = (C::PART_NCH_MAX + 1) / 2;
     uint32_t dq_cnt = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int pos = zigzag_pos(round, blockIdx.x, G);
       if (pos >= n_work) break;
-      const BwdItem it = bwd_decode(args, pos);
+      const BwdItem it = bwd_decode(args, pos, C::NPART);
+      // this item's dQ columns: [128 part, 128 part + 32 nch)
+      const int nch = (item_part<C>(it) == 0 ? C::PART_COLS0 : C::PART_COLS1) / 32, npair = (nch + 1) / 2;
+      const int coff = item_part<C>(it) * 128;
       for (int s = 0; s < it.nsteps; ++s) {
         int h, q0;
         bwd_step(it, pb, s, h, q0);
@@ -655,24 +709,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // 32 columns a chunk, written as paired 32-byte stores
           using T = typename std::conditional<C::DT == DT_FP16, __half, __nv_bfloat16>::type;
           T* drow_out = reinterpret_cast<T*>(args.dq) +
-                        (static_cast<size_t>(it.q_start + q0 + row) * pb.h_q + h) * C::DQK;
+                        (static_cast<size_t>(it.q_start + q0 + row) * pb.h_q + h) * C::DQK + coff;
           const bool v8 = (reinterpret_cast<uintptr_t>(args.dq) & 31) == 0;
           const size_t stride = static_cast<size_t>(pb.h_q) * C::DQK * sizeof(T);
 #pragma unroll
-          for (int pr = 0; pr < NPAIR; ++pr) {
+          for (int pr = 0; pr < NPAIR_MAX; ++pr) {
+            if (pr >= npair) break;
             const int c0 = 2 * pr;
             uint32_t a[32], b[32];
             tmem_ld32(t_dq + c0 * 32, a);
-            if (c0 + 1 < NCH) tmem_ld32(t_dq + (c0 + 1) * 32, b);
+            if (c0 + 1 < nch) tmem_ld32(t_dq + (c0 + 1) * 32, b);
             tmem_ld_wait(a);
-            if (c0 + 1 < NCH) tmem_ld_wait(b);
-            if (pr == NPAIR - 1) {
+            if (c0 + 1 < nch) tmem_ld_wait(b);
+            if (pr == npair - 1) {
               tc_fence_before();
               mbar_arrive(&sm.dq_empty);  // every TMEM read of this tile is done
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              if (c0 + half >= NCH) break;
+              if (c0 + half >= nch) break;
               const uint32_t(&o)[32] = half == 0 ? a : b;
               uint32_t w[16];
 #pragma unroll
@@ -693,13 +748,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // deterministic mode: this key block's dQ tile goes to its own slice; a
           // later kernel adds the slices in key-block order
           float* dst = args.dq_part + ((static_cast<size_t>(it.k0 / kTileK) * pb.total_q + it.q_start + q0 + row) *
-                                           pb.h_q + h) * C::DQK;
+                                           pb.h_q + h) * C::DQK + coff;
 #pragma unroll 1
-          for (int ch = 0; ch < C::DQK / 32; ++ch) {
+          for (int ch = 0; ch < nch; ++ch) {
             uint32_t o[32];
             tmem_ld32(t_dq + ch * 32, o);
             tmem_ld_wait(o);
-            if (ch == C::DQK / 32 - 1) {
+            if (ch == nch - 1) {
               tc_fence_before();
               mbar_arrive(&sm.dq_empty);
             }
@@ -724,22 +779,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         };
         auto reduce_pair = [&](int c0) {  // lane 0: add boxes 0 (and 1) into chunks c0 (and c0 + 1), one bulk group
-          tma_reduce_add_3d(&tm_dq, stage_base, c0 * 32, h, it.q_start + q0 + quad * 32);
-          if (c0 + 1 < NCH) tma_reduce_add_3d(&tm_dq, stage_base + C::DQ_CHUNK_BYTES, (c0 + 1) * 32, h,
+          tma_reduce_add_3d(&tm_dq, stage_base, coff + c0 * 32, h, it.q_start + q0 + quad * 32);
+          if (c0 + 1 < nch) tma_reduce_add_3d(&tm_dq, stage_base + C::DQ_CHUNK_BYTES, coff + (c0 + 1) * 32, h,
                                               it.q_start + q0 + quad * 32);
           bulk_commit_group();
         };
         if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's reduces are done reading both boxes
         __syncwarp();
 #pragma unroll
-        for (int pr = 0; pr < NPAIR; ++pr) {
+        for (int pr = 0; pr < NPAIR_MAX; ++pr) {
+          if (pr >= npair) break;
           const int c0 = 2 * pr;
           uint32_t a[32], b[32];
           tmem_ld32(t_dq + c0 * 32, a);
-          if (c0 + 1 < NCH) tmem_ld32(t_dq + (c0 + 1) * 32, b);
+          if (c0 + 1 < nch) tmem_ld32(t_dq + (c0 + 1) * 32, b);
           tmem_ld_wait(a);
-          if (c0 + 1 < NCH) tmem_ld_wait(b);
-          if (pr == NPAIR - 1) {
+          if (c0 + 1 < nch) tmem_ld_wait(b);
+          if (pr == npair - 1) {
             tc_fence_before();
             mbar_arrive(&sm.dq_empty);  // every TMEM read of this tile is done
           }
@@ -751,11 +807,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             __syncwarp();
           }
           stage(0, a);
-          if (c0 + 1 < NCH) stage(1, b);
+          if (c0 + 1 < nch) stage(1, b);
           fence_async_shared();
           __syncwarp();
         }
-        if (lane == 0) reduce_pair(2 * (NPAIR - 1));
+        if (lane == 0) reduce_pair(2 * (npair - 1));
         }  // not C::DIRECT_DQ
       }
     }

@@ -24,10 +24,12 @@ LENS_K = [300, 129, 5, 40, 0, 512]
         (64, 4, 1, "relu2", True, 100),
         (96, 2, 2, "gelu_tanh", False, 60),
         (128, 2, 2, "softmax", True, -1),
+        (192, 4, 2, "fast_gelu", True, 150),
     ],
 )
 def test_deterministic_backward_matches_oracle_and_repeats_bitwise(d, h_q, h_kv, act, causal, window):
-    inp = inputs.custom(len(LENS_Q), h_q, h_kv, d, d, LENS_Q, LENS_K, act, causal=causal, window=window, seed=11)
+    dv_ = 128 if d == 192 else d  # (192, 128): dK and dQ in two column parts
+    inp = inputs.custom(len(LENS_Q), h_q, h_kv, d, dv_, LENS_Q, LENS_K, act, causal=causal, window=window, seed=11)
     out, lse = run_fwd(inp) if act == "softmax" else (None, None)
     dq, dk, dv = run_bwd(inp, out, lse, deterministic=True)
     rq, rk, rv = ref_bwd(inp)

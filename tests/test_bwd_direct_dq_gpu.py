@@ -42,12 +42,14 @@ def _bwd_into(inp, out, lse, deterministic, sentinel=7.0, max_k=None):
         (2, 2, 96, "gelu_tanh", False, 30, "bf16"),
         (2, 2, 128, "softmax", True, -1, "bf16"),
         (2, 2, 128, "identity", False, -1, "fp16"),
+        (4, 2, 192, "gelu", True, 50, "bf16"),
     ],
 )
 @pytest.mark.parametrize("deterministic", [False, True])
 def test_direct_dq_matches_oracle_and_writes_every_row(h_q, h_kv, d, act, causal, window, dtype, deterministic):
     ensure_built()
-    inp = inputs.custom(len(LQ), h_q, h_kv, d, d, LQ, LK, act, causal=causal, window=window, dtype=dtype, seed=21)
+    dv_ = 128 if d == 192 else d  # (192, 128): dQ written by two column-part items
+    inp = inputs.custom(len(LQ), h_q, h_kv, d, dv_, LQ, LK, act, causal=causal, window=window, dtype=dtype, seed=21)
     out, lse = run_fwd(inp) if act == "softmax" else (None, None)
     dq, dk, dv = _bwd_into(inp, out, lse, deterministic)
     assert _lib.gdpa_get_status() == 0

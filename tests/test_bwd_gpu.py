@@ -43,7 +43,7 @@ def test_masks_and_heads(causal, window, h_kv):
            f"causal={causal} window={window} h_kv={h_kv}")
 
 
-@pytest.mark.parametrize("dims", [(64, 64), (96, 96)])
+@pytest.mark.parametrize("dims", [(64, 64), (96, 96), (192, 128)])
 @pytest.mark.parametrize("act", ["gelu", "softmax"])
 def test_head_dims(dims, act):
     lens = [130, 1, 256, 300, 77]
@@ -65,3 +65,20 @@ def test_empty_and_unseen_blocks_give_zero_gradients():
     assert torch.count_nonzero(dk[:10]) == 0 and torch.count_nonzero(dv[:10]) == 0
     for g, r, n in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
         assert_close(g, r, GRAD_TOL, n)
+
+
+# (192, 128): dK and dQ come from two column-part work items ([0, 128) with
+# dV, and [128, 192)); GQA and MQA groups, causal and sliding-window masks on
+# ragged lengths that leave key blocks without queries and queries without keys.
+@pytest.mark.parametrize("act,causal,window,h_kv,dtype", [
+    ("silu", True, 37, 2, "bf16"),
+    ("fast_gelu", True, -1, 1, "bf16"),
+    ("relu2", False, 200, 4, "bf16"),
+    ("hardswish", False, -1, 2, "fp16"),
+    ("softmax", True, 130, 2, "bf16"),
+])
+def test_d192(act, causal, window, h_kv, dtype):
+    lq = [100, 257, 3, 0, 130, 129, 400]
+    lk = [300, 257, 0, 5, 64, 400, 129]
+    _check(inputs.custom(len(lq), 4, h_kv, 192, 128, lq, lk, act, causal=causal, window=window, dtype=dtype, seed=16),
+           f"d192 {act} causal={causal} window={window} h_kv={h_kv} {dtype}")

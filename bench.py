@@ -2,8 +2,8 @@
 """GDPA forward + backward throughput on GB300 (useful TFLOP/s).
 
 One step = the whole hot path over one batch of synthetic input, through the
-C-ABI: gdpa_fwd (work list, forward kernel) then gdpa_bwd (work list, dQ
-clear, backward kernel, dQ convert). The workload is the jagged
+C-ABI: gdpa_fwd (work list, forward kernel) then gdpa_bwd (work list and dQ
+clear in one launch, backward kernel, dQ convert). The workload is the jagged
 self-attention scenario of the gdpa/README.md page's benchmark section
 ("Self Attention, sparsity=0.5"): B=64 sequences with lengths uniform in
 [1, 2048], 4 heads, head dim 128, bf16, GELU, non-causal.
@@ -491,9 +491,11 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # per step: work list + forward kernel; backward: work list, prep, main kernel and (unless dQ
-        # is written directly) the dQ convert
-        "gpu_launches": (2 + (0 if fwd_only else (3 if mk <= 128 else 4))) * K,
+        # per step: work list + forward kernel; backward: work list (which also clears the dQ
+        # accumulator), prep (softmax rowsum, or direct dQ's unwritten rows), main kernel and (unless
+        # dQ is written directly) the dQ convert
+        "gpu_launches": (2 + (0 if fwd_only else 2 + (1 if (wl.act == "softmax" or mk <= 128) else 0)
+                              + (1 if mk > 128 else 0))) * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

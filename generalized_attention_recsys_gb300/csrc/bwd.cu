@@ -1,5 +1,6 @@
-// Backward launcher: clears the fp32 dQ accumulator (and, for softmax,
-// computes rowsum(dO * O)), runs the main kernel, then converts dQ; in
+// Backward launcher: for softmax computes rowsum(dO * O) (and, with direct dQ,
+// zeroes the dq rows no work item writes), runs the main kernel, then
+// converts the fp32 dQ accumulator (cleared by the work-list launch); in
 // deterministic mode it adds the per-key-block dQ slices in a fixed order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -33,17 +34,15 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 template <>
 __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 
-// Zero the dQ accumulator (n4 float4s; 0 when there is none); softmax:
-// drow[h, t] = sum_d dO[t, h, d] * O[t, h, d]. With direct dQ (zero_dq set),
+// Softmax: drow[h, t] = sum_d dO[t, h, d] * O[t, h, d]. With direct dQ (zero_dq set),
 // the rows of query blocks that no work item visits are zeroed in dq itself
 // (every sequence has at most one key block, covering the query blocks that
 // query_range gives; the kernel writes the rest).
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_prep(float4* acc, size_t n4, const T* out, const T* dout, float* drow,
-                                                int total_q, int h_q, int d_v, Problem pb, T* zero_dq, int d_qk) {
+__global__ void __launch_bounds__(256) bwd_prep(const T* out, const T* dout, float* drow, int total_q, int h_q,
+                                                int d_v, Problem pb, T* zero_dq, int d_qk) {
   const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
   const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t i = tid; i < n4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (zero_dq != nullptr) {
     const size_t row_elems = static_cast<size_t>(h_q) * d_qk;  // one token: every head
     for (int b = static_cast<int>(tid / 32); b < pb.batch; b += static_cast<int>(nthr / 32)) {
@@ -163,21 +162,21 @@ __global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T*
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdq, const BwdArgs& a, int grid, cudaStream_t stream, cudaEvent_t before,
                        cudaEvent_t after) {
-  // only the accumulating mode has an accumulator to clear
-  const size_t n4 = a.dq_mode == DQ_ACCUMULATE ? static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4 : 0;
+  // (the accumulating mode's accumulator was cleared by the work-list launch)
   const bool direct = a.dq_mode == DQ_DIRECT;
+  const size_t n4_post = a.dq_mode == DQ_ACCUMULATE ? static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4 : 0;
   const int eg = grid * 8;  // elementwise kernels: 8 blocks of 256 per SM
   float* drow = a.act == ACT_SOFTMAX ? a.drow : nullptr;
-  if (a.dtype == DT_FP16)
-    bwd_prep<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<float4*>(a.dq_acc), n4,
-                                             static_cast<const __half*>(a.out), static_cast<const __half*>(a.dout),
+  if (drow == nullptr && !direct) {
+    // nothing to prepare
+  } else if (a.dtype == DT_FP16)
+    bwd_prep<__half><<<eg, 256, 0, stream>>>(static_cast<const __half*>(a.out), static_cast<const __half*>(a.dout),
                                              drow, a.pb.total_q, a.pb.h_q, a.d_v, a.pb,
                                              direct ? static_cast<__half*>(a.dq) : nullptr, a.d_qk);
   else
     bwd_prep<__nv_bfloat16><<<eg, 256, 0, stream>>>(
-        reinterpret_cast<float4*>(a.dq_acc), n4, static_cast<const __nv_bfloat16*>(a.out),
-        static_cast<const __nv_bfloat16*>(a.dout), drow, a.pb.total_q, a.pb.h_q, a.d_v, a.pb,
-        direct ? static_cast<__nv_bfloat16*>(a.dq) : nullptr, a.d_qk);
+        static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), drow, a.pb.total_q,
+        a.pb.h_q, a.d_v, a.pb, direct ? static_cast<__nv_bfloat16*>(a.dq) : nullptr, a.d_qk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (before) cudaEventRecord(before, stream);
@@ -201,10 +200,10 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     return cudaGetLastError();
   }
   if (a.dtype == DT_FP16)
-    bwd_post<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4,
+    bwd_post<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4_post,
                                              static_cast<__half*>(a.dq));
   else
-    bwd_post<__nv_bfloat16><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4,
+    bwd_post<__nv_bfloat16><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4_post,
                                                     static_cast<__nv_bfloat16*>(a.dq));
   return cudaGetLastError();
 }

@@ -195,6 +195,8 @@ __device__ __forceinline__ int seq_bucket(const Problem& pb, int mode, int nblk,
 // backward's dQ accumulator) meanwhile, so that clear needs no launch of its own.
 __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, WorkList* wl, int cap, float4* clear,
                                                        size_t n4) {
+  pdl_wait();  // the workspace may still be in use by the previous kernel
+  pdl_release();
   if (blockIdx.x > 0) {
     const size_t nthr = static_cast<size_t>(gridDim.x - 1) * blockDim.x;
     for (size_t i = (blockIdx.x - 1) * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += nthr)
@@ -337,8 +339,9 @@ int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   const Problem pb = make_problem(s, cu_q, cu_k, max_q, max_k, causal, window);
   WorkList* wl = static_cast<WorkList*>(workspace);
   const int cap = static_cast<int>(fwd_list_cap(s));
-  build_worklist<<<1, 1024, 0, stream>>>(pb, 0, wl, cap, nullptr, 0);
-  if (cudaGetLastError() != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_pdl(build_worklist, dim3(1), dim3(1024), 0, stream, pb, 0, wl, cap, static_cast<float4*>(nullptr),
+                 static_cast<size_t>(0)) != cudaSuccess)
+    return GDPA_ERR_CUDA;
 
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, s->total_q, s->h_q, s->d_qk, s->dtype, workspace) ||
@@ -409,8 +412,9 @@ int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   // one key block per sequence (direct dQ) or deterministic slices: no accumulator to clear
   const bool accumulate = max_k > kTileK && !deterministic;
   const size_t n4 = accumulate ? static_cast<size_t>(s->total_q) * s->h_q * s->d_qk / 4 : 0;
-  build_worklist<<<n4 > 0 ? 1 + 2 * nsm : 1, 1024, 0, stream>>>(pb, 1, wl, cap, reinterpret_cast<float4*>(dq_acc), n4);
-  if (cudaGetLastError() != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_pdl(build_worklist, dim3(n4 > 0 ? 1 + 2 * nsm : 1), dim3(1024), 0, stream, pb, 1, wl, cap,
+                 reinterpret_cast<float4*>(dq_acc), n4) != cudaSuccess)
+    return GDPA_ERR_CUDA;
 
   BwdArgs a;
   a.pb = pb;

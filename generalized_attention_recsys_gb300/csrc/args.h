@@ -12,6 +12,26 @@
 
 namespace gdpa {
 
+// Launches `kernel` with programmatic dependent launch allowed (see
+// pdl_wait in common.cuh): its blocks may start, and run up to pdl_wait,
+// while the previous kernel on the stream is still finishing.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+
 namespace {
 // Sets a kernel's dynamic shared-memory limit once per device (attributes
 // are per device). Internal linkage on purpose: a static local of a function

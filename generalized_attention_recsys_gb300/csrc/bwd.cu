@@ -41,6 +41,8 @@ __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_prep(const T* out, const T* dout, float* drow, int total_q, int h_q,
                                                 int d_v, Problem pb, T* zero_dq, int d_qk) {
+  pdl_wait();
+  pdl_release();
   const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
   const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
   if (zero_dq != nullptr) {
@@ -109,6 +111,8 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
 // items use, so only written slices are read). One warp per row.
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Problem pb, int d, int n_slices, T* dq) {
+  pdl_wait();
+  pdl_release();
   const int lane = threadIdx.x & 31;
   const size_t nwarps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
   const size_t rows = static_cast<size_t>(pb.total_q) * pb.h_q;
@@ -152,6 +156,8 @@ __global__ void __launch_bounds__(256) bwd_post_ordered(const float* part, Probl
 
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_post(const float4* acc, size_t n4, T* dq) {
+  pdl_wait();
+  pdl_release();
   const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
   const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = tid; i < n4; i += nthr) store4<T>(dq + 4 * i, acc[i]);
@@ -167,17 +173,19 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   const size_t n4_post = a.dq_mode == DQ_ACCUMULATE ? static_cast<size_t>(a.pb.total_q) * a.pb.h_q * a.d_qk / 4 : 0;
   const int eg = grid * 8;  // elementwise kernels: 8 blocks of 256 per SM
   float* drow = a.act == ACT_SOFTMAX ? a.drow : nullptr;
+  cudaError_t e = cudaSuccess;
   if (drow == nullptr && !direct) {
     // nothing to prepare
-  } else if (a.dtype == DT_FP16)
-    bwd_prep<__half><<<eg, 256, 0, stream>>>(static_cast<const __half*>(a.out), static_cast<const __half*>(a.dout),
-                                             drow, a.pb.total_q, a.pb.h_q, a.d_v, a.pb,
-                                             direct ? static_cast<__half*>(a.dq) : nullptr, a.d_qk);
-  else
-    bwd_prep<__nv_bfloat16><<<eg, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), drow, a.pb.total_q,
-        a.pb.h_q, a.d_v, a.pb, direct ? static_cast<__nv_bfloat16*>(a.dq) : nullptr, a.d_qk);
-  cudaError_t e = cudaGetLastError();
+  } else if (a.dtype == DT_FP16) {
+    e = launch_pdl(bwd_prep<__half>, dim3(eg), dim3(256), 0, stream, static_cast<const __half*>(a.out),
+                   static_cast<const __half*>(a.dout), drow, a.pb.total_q, a.pb.h_q, a.d_v, a.pb,
+                   direct ? static_cast<__half*>(a.dq) : nullptr, a.d_qk);
+  } else {
+    e = launch_pdl(bwd_prep<__nv_bfloat16>, dim3(eg), dim3(256), 0, stream,
+                   static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), drow,
+                   a.pb.total_q, a.pb.h_q, a.d_v, a.pb, direct ? static_cast<__nv_bfloat16*>(a.dq) : nullptr,
+                   a.d_qk);
+  }
   if (e != cudaSuccess) return e;
   if (before) cudaEventRecord(before, stream);
   switch (a.d_qk) {
@@ -192,20 +200,17 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (direct) return cudaSuccess;  // dQ is already in place
   if (a.dq_mode == DQ_SLICES) {
     if (a.dtype == DT_FP16)
-      bwd_post_ordered<__half><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk, a.n_kblocks,
-                                                     static_cast<__half*>(a.dq));
-    else
-      bwd_post_ordered<__nv_bfloat16><<<eg, 256, 0, stream>>>(a.dq_part, a.pb, a.d_qk, a.n_kblocks,
-                                                             static_cast<__nv_bfloat16*>(a.dq));
-    return cudaGetLastError();
+      return launch_pdl(bwd_post_ordered<__half>, dim3(eg), dim3(256), 0, stream, static_cast<const float*>(a.dq_part),
+                        a.pb, a.d_qk, a.n_kblocks, static_cast<__half*>(a.dq));
+    return launch_pdl(bwd_post_ordered<__nv_bfloat16>, dim3(eg), dim3(256), 0, stream,
+                      static_cast<const float*>(a.dq_part), a.pb, a.d_qk, a.n_kblocks,
+                      static_cast<__nv_bfloat16*>(a.dq));
   }
   if (a.dtype == DT_FP16)
-    bwd_post<__half><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4_post,
-                                             static_cast<__half*>(a.dq));
-  else
-    bwd_post<__nv_bfloat16><<<eg, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc), n4_post,
-                                                    static_cast<__nv_bfloat16*>(a.dq));
-  return cudaGetLastError();
+    return launch_pdl(bwd_post<__half>, dim3(eg), dim3(256), 0, stream, reinterpret_cast<const float4*>(a.dq_acc),
+                      n4_post, static_cast<__half*>(a.dq));
+  return launch_pdl(bwd_post<__nv_bfloat16>, dim3(eg), dim3(256), 0, stream,
+                    reinterpret_cast<const float4*>(a.dq_acc), n4_post, static_cast<__nv_bfloat16*>(a.dq));
 }
 
 }  // namespace gdpa

@@ -358,6 +358,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  pdl_wait();  // the work list, the cleared accumulator and the inputs come from earlier kernels
+  pdl_release();
   // registers: control warpgroup 96, elementwise warpgroups 160, drain warpgroup 96
   // (128 * 96 + 256 * 160 + 128 * 96 = 65536 = 512 * 128 launched)
   static_assert(C::NG == 2 && C::THREADS == 512, "register split assumes two elementwise warpgroups");
@@ -852,8 +854,7 @@ cudaError_t launch_bwd_kernel(const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < 128) return cudaErrorInvalidConfiguration;
   const cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, tq, tk, tv, tdo, tdq, a);
 }
 
 template <int DQK, int DV, int DT>

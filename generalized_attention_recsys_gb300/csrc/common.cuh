@@ -12,6 +12,15 @@ constexpr int kFwdItemRows = kTileQ;  // a forward work item is one Q tile of on
 
 enum DType : int { DT_BF16 = 0, DT_FP16 = 1, DT_E4M3 = 2 };
 
+// Programmatic dependent launch. Every kernel of the library is launched so
+// that it may start while the previous kernel on the stream finishes; it
+// calls pdl_wait() before it reads or writes memory that an earlier kernel
+// may still use (the wait returns once that kernel has completed and its
+// writes are visible; without a programmatic predecessor it returns at
+// once), and pdl_release() to let the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 struct Problem {
   int batch, total_q, total_k;
   int h_q, h_kv, group;  // group = h_q / h_kv

@@ -454,6 +454,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  pdl_wait();  // the work list and inputs come from earlier kernels; out may still be read
+  pdl_release();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producers: the K ring (lane 0) and Q tiles (lane 1)
@@ -988,8 +990,7 @@ cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   auto kern = gdpa_fwd_kernel<C>;
   const cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, tq, tk, tv, a);
 }
 
 template <int DQK, int DV, int DT>

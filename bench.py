@@ -453,6 +453,14 @@ def main():
                  (esz(out) + esz(lse) if lse is not None else 0))
     dom_bytes = bwd_bytes if dominant == "gdpa_bwd_kernel" else fwd_bytes
     hbm = float(peaks["hbm_gbs"])
+    # each main kernel against both ceilings: algorithmic bytes (and FLOPs) per launch / its event time
+    kernels = {"gdpa_fwd_kernel": {"ms": fwd_ms, "tflops": fwd_tflops, "gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9,
+                                   "hbm_frac": fwd_bytes / (fwd_ms * 1e-3) / 1e9 / hbm,
+                                   "algorithmic_bytes": fwd_bytes}}
+    if not fwd_only:
+        kernels["gdpa_bwd_kernel"] = {"ms": bwd_ms, "tflops": bwd_tflops, "gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
+                                      "hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / hbm,
+                                      "algorithmic_bytes": bwd_bytes}
     if dom_flops / dom_bytes < peak * 1e12 / (hbm * 1e9):  # below the ridge point: bound by HBM
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -489,6 +497,7 @@ def main():
         "peak_bf16_tflops": {"burst": peak, "sustained": float(peaks.get("bf16_tflops_sustained", 0.0)),
                              "source": peak_src},
         "roofline": roofline,
+        "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
         # per step: work list + forward kernel; backward: work list (which also clears the dQ

@@ -302,7 +302,8 @@ def main():
     cu_q, cu_k = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
     mq, mk = inp.max_q, inp.max_k
     desc = torch.tensor(inp.descale, dtype=torch.float32, device=dev) if inp.descale is not None else None
-    out_dtype = torch.bfloat16 if wl.dtype == "e4m3" else q.dtype
+    mxs = tuple(t.to(dev) for t in inp.mx) if inp.mx is not None else None  # MXFP8 block scales of q, k, v
+    out_dtype = torch.bfloat16 if wl.dtype in ("e4m3", "mxe4m3") else q.dtype
     out = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=out_dtype, device=dev)
     lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=dev) if wl.act == "softmax" else None
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -312,12 +313,18 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     a = (wl.act, wl.softmax_scale, wl.causal, wl.window)
 
+    def fwd_call(qq, kk, vv, cq, ck, o, l, sc):
+        if sc is not None:
+            _lib.gdpa_fwd_mxfp8(qq, kk, vv, *sc, cq, ck, mq, mk, *a, out=o, lse=l, batch=wl.batch, workspace=ws_f)
+        else:
+            _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, descale_qkv=desc, out=o, lse=l, batch=wl.batch,
+                          workspace=ws_f)
+
     def step(qq=q, kk=k, vv=v, dd=do, cq=cu_q, ck=cu_k, ev=None, o=None):
         o = out if o is None else o
         if ev is not None:
             _lib.gdpa_set_profile_events(ev[0], ev[1])
-        _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, descale_qkv=desc, out=o, lse=lse, batch=wl.batch,
-                      workspace=ws_f)
+        fwd_call(qq, kk, vv, cq, ck, o, lse, mxs)
         if not fwd_only:
             if ev is not None:
                 _lib.gdpa_set_profile_events(ev[2], ev[3])
@@ -371,7 +378,9 @@ def main():
     e2e = None
     if not args.no_e2e:
         # inputs q, k, v, (dO), cu_seqlens; results out, (lse), (dq, dk, dv)
-        ins = [inp.q, inp.k, inp.v] + ([inp.dout] if not fwd_only else []) + [inp.cu_seqlens_q, inp.cu_seqlens_k]
+        ins = ([inp.q, inp.k, inp.v] + ([inp.dout] if not fwd_only else []) + [inp.cu_seqlens_q, inp.cu_seqlens_k] +
+               (list(inp.mx) if inp.mx is not None else []))
+        n_mx = 3 if inp.mx is not None else 0
         host_in = [t.pin_memory() for t in ins]
         dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
         res = [out] + ([lse] if lse is not None else []) + ([dq, dk, dv] if not fwd_only else [])
@@ -398,11 +407,11 @@ def main():
                 comp.wait_event(out_done[b])  # step i-2's results have left these buffers
                 qq, kk, vv = dev_in[b][:3]
                 dd = dev_in[b][3] if not fwd_only else None
-                cq, ck = dev_in[b][-2:]
+                nin = len(dev_in[b]) - n_mx
+                cq, ck = dev_in[b][nin - 2:nin]
                 r = dev_out[b]
                 o_, l_ = r[0], (r[1] if lse is not None else None)
-                _lib.gdpa_fwd(qq, kk, vv, cq, ck, mq, mk, *a, descale_qkv=desc, out=o_, lse=l_, batch=wl.batch,
-                              workspace=ws_f)
+                fwd_call(qq, kk, vv, cq, ck, o_, l_, tuple(dev_in[b][nin:]) if n_mx else None)
                 if not fwd_only:
                     dq_, dk_, dv_ = r[-3:]
                     _lib.gdpa_bwd(qq, kk, vv, cq, ck, mq, mk, *a, o_, l_, dd, dq=dq_, dk=dk_, dv=dv_,
@@ -439,7 +448,7 @@ def main():
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     peak_label = f"{peak_src} bf16 dense (burst)"
-    if wl.dtype == "e4m3":  # the contraction's own dtype: measured bf16 x the nominal e4m3 / bf16 ratio (4.5 / 2.25)
+    if wl.dtype in ("e4m3", "mxe4m3"):  # the contraction's dtype: measured bf16 x the nominal e4m3 / bf16 ratio (4.5 / 2.25)
         peak *= 2.0
         peak_label = f"{peak_src} bf16 dense (burst) x 2, the nominal e4m3 / bf16 ratio"
     fwd_tflops = f_fwd / (fwd_ms * 1e-3) / 1e12

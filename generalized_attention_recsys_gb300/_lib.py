@@ -69,6 +69,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdpa_error_string.restype = ctypes.c_char_p
         lib.gdpa_set_profile_events.argtypes = [vp, vp]
         lib.gdpa_set_profile_events.restype = ci
+        lib.gdpa_fwd_mxfp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, cf, ci, ci, vp, vp, vp, sz,
+                                       vp]
+        lib.gdpa_fwd_mxfp8.restype = ci
         lib.gdpa_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, ci, ci, ci, cf, ci, ci, vp, vp, vp, vp]
         lib.gdpa_fwd_noalloc.restype = ci
         lib.gdpa_num_sms.argtypes = []
@@ -145,6 +148,33 @@ def gdpa_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_
                       int(max_seqlen_q), int(max_seqlen_k), a, float(scale), int(bool(causal)), int(window),
                       _ptr(descale_qkv), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
                       _stream(stream))
+    _check(st)
+    return out, (lse if a == ACTS["softmax"] else None)
+
+
+def gdpa_fwd_mxfp8(q, k, v, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                   max_seqlen_k: int, act, scale: float, causal: bool = False, window: int = -1, out=None, lse=None,
+                   batch=None, workspace=None, stream=None):
+    """C-ABI gdpa_fwd_mxfp8: q, k, v e4m3 codes; q_scale / k_scale [tokens, heads, d_qk / 32] and
+    v_scale [ceil(total_k / 32), h_kv, d_v] E8M0 bytes (uint8). Returns (out, lse)."""
+    lib = load()
+    if batch is None:
+        batch = cu_seqlens_q.numel() - 1 if cu_seqlens_q is not None else q.shape[0] // max(max_seqlen_q, 1)
+    shape = make_shape(q, k, v, batch)
+    a = _act(act)
+    if out is None:
+        out = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=torch.bfloat16, device=q.device)
+    if a == ACTS["softmax"] and lse is None:
+        lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    for t in (q_scale, k_scale, v_scale):
+        if t is not None and t.dtype != torch.uint8:
+            raise TypeError("MX scales are E8M0 bytes (torch.uint8)")
+    nb = gdpa_workspace_bytes(shape, max_seqlen_q, max_seqlen_k, False)
+    ws = _workspace(nb, q.device, workspace)
+    st = lib.gdpa_fwd_mxfp8(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale),
+                            _ptr(v_scale), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q),
+                            int(max_seqlen_k), a, float(scale), int(bool(causal)), int(window), _ptr(out), _ptr(lse),
+                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(st)
     return out, (lse if a == ACTS["softmax"] else None)
 

@@ -316,19 +316,32 @@ size_t gdpa_workspace_bytes(const gdpa_shape* s, int max_q, int max_k, int is_bw
   return b;
 }
 
-int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, const int32_t* cu_q,
-             const int32_t* cu_k, int max_q, int max_k, int act, float scale, int causal, int window,
-             const float* descale, void* out, float* lse, void* workspace, size_t workspace_bytes,
-             void* stream_) {
+}  // extern "C"
+
+namespace {
+
+// The forward of gdpa_fwd (descale for e4m3) and gdpa_fwd_mxfp8 (sf_q/k/v).
+int fwd_common(const gdpa_shape* s, const void* q, const void* k, const void* v, const int32_t* cu_q,
+               const int32_t* cu_k, int max_q, int max_k, int act, float scale, int causal, int window,
+               const float* descale, const uint8_t* sf_q, const uint8_t* sf_k, const uint8_t* sf_v, void* out,
+               float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
   int st = validate(s, max_q, max_k, act, causal, window);
   if (st != GDPA_OK) return st;
+  const bool mx = sf_q != nullptr;
+  if (mx) {
+    if (s->dtype != GDPA_E4M3) return GDPA_ERR_INVALID;
+    if (!((s->d_qk == 128 || s->d_qk == 192) && s->d_v == 128)) return GDPA_ERR_UNSUPPORTED;
+    if (s->total_k > 0 && (!sf_k || !sf_v)) return GDPA_ERR_INVALID;
+    if (!aligned16(sf_q) || (sf_k && !aligned16(sf_k)) || (sf_v && !aligned16(sf_v))) return GDPA_ERR_INVALID;
+    if (!cu_k && max_k % 32 != 0) return GDPA_ERR_INVALID;  // fixed length: every key sequence starts on a block
+  }
   if (s->total_q == 0 || s->batch == 0) return GDPA_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return GDPA_ERR_INVALID;
   if (s->total_k > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return GDPA_ERR_INVALID;
   if ((cu_q == nullptr) != (cu_k == nullptr)) return GDPA_ERR_INVALID;
   if (!cu_q && (s->total_q != s->batch * max_q || s->total_k != s->batch * max_k)) return GDPA_ERR_INVALID;
   if (act == GDPA_ACT_SOFTMAX && !lse) return GDPA_ERR_INVALID;
-  if (s->dtype == GDPA_E4M3 && !descale) return GDPA_ERR_INVALID;
+  if (s->dtype == GDPA_E4M3 && !descale && !mx) return GDPA_ERR_INVALID;
   if (!workspace || !aligned16(workspace) || workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, 0))
     return GDPA_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -353,7 +366,10 @@ int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   a.pb = pb;
   a.act = act;
   a.scale = scale;
-  a.descale = descale;
+  a.descale = mx ? nullptr : descale;
+  a.sf_q = sf_q;
+  a.sf_k = mx ? sf_k : nullptr;
+  a.sf_v = mx ? sf_v : nullptr;
   a.out = out;
   a.lse = lse;
   a.work = wl;
@@ -371,6 +387,27 @@ int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, c
   }
   mark(t_ev_after, stream);
   return e == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdpa_fwd(const gdpa_shape* s, const void* q, const void* k, const void* v, const int32_t* cu_q,
+             const int32_t* cu_k, int max_q, int max_k, int act, float scale, int causal, int window,
+             const float* descale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+             void* stream_) {
+  return fwd_common(s, q, k, v, cu_q, cu_k, max_q, max_k, act, scale, causal, window, descale, nullptr, nullptr,
+                    nullptr, out, lse, workspace, workspace_bytes, stream_);
+}
+
+int gdpa_fwd_mxfp8(const gdpa_shape* s, const void* q, const void* k, const void* v, const uint8_t* q_scale,
+                   const uint8_t* k_scale, const uint8_t* v_scale, const int32_t* cu_q, const int32_t* cu_k, int max_q,
+                   int max_k, int act, float scale, int causal, int window, void* out, float* lse, void* workspace,
+                   size_t workspace_bytes, void* stream_) {
+  if (!q_scale) return GDPA_ERR_INVALID;
+  return fwd_common(s, q, k, v, cu_q, cu_k, max_q, max_k, act, scale, causal, window, nullptr, q_scale, k_scale,
+                    v_scale, out, lse, workspace, workspace_bytes, stream_);
 }
 
 int gdpa_bwd(const gdpa_shape* s, const void* q, const void* k, const void* v, const int32_t* cu_q,

@@ -58,6 +58,11 @@ struct FwdArgs {
   int act;
   float scale;
   const float* descale;  // e4m3: (q, k, v) per-tensor scales; else NULL
+  // MXFP8 (e4m3 codes with E8M0 block scales; NULL otherwise): q [total_q, h_q, d_qk / 32] and
+  // k [total_k, h_kv, d_qk / 32] per 32 head-dim elements, v [ceil(total_k / 32), h_kv, d_v] per 32 keys
+  const uint8_t* sf_q;
+  const uint8_t* sf_k;
+  const uint8_t* sf_v;
   void* out;             // [total_q, h_q, dv]; bf16 for bf16/e4m3 inputs, f16 for f16
   float* lse;            // [h_q, total_q] (softmax)
   const WorkList* work;

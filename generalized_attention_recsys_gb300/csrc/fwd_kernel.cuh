@@ -62,10 +62,18 @@ __host__ __device__ constexpr int fwd_ring_stages(int avail, int per, int cap) {
   return avail / per > cap ? cap : avail / per;
 }
 
-template <int DQK_, int DV_, int DT_, int NG_, bool SOFTMAX_ = false>
+template <int DQK_, int DV_, int DT_, int NG_, bool SOFTMAX_ = false, bool MX_ = false>
 struct FwdCfg {
   static constexpr int DQK = DQK_, DV = DV_, DT = DT_, NG = NG_;
   static constexpr bool SOFTMAX = SOFTMAX_;
+  // MXFP8: e4m3 codes with one E8M0 scale per 32 elements along each GEMM's K
+  // (see FwdArgs::sf_q); the MMAs apply the scales (kind::mxf8f6f4).
+  static constexpr bool MX = MX_;
+  static_assert(!MX || (DT_ == DT_E4M3 && DQK_ % 32 == 0 && DV_ == 128), "MXFP8: e4m3, d_qk % 32 == 0, d_v = 128");
+  // scale-factor atoms (512 bytes: 128 rows x 4 K blocks) per Q / K tile and per V tile
+  static constexpr int NQB = (DQK_ / 32 + 3) / 4;
+  static constexpr int SF_ATOM = 512;
+  static constexpr int SF_RESERVE = MX ? (2 + 4) * NQB * SF_ATOM + 4 * SF_ATOM + SF_ATOM : 0;
   static_assert(!SOFTMAX || NG == 2, "softmax runs with two activation groups");
   static constexpr int ESZ = DT == DT_E4M3 ? 1 : 2;
   static constexpr int BOX_ELEMS = 128 / ESZ;  // elements per 128-byte swizzle row
@@ -81,7 +89,7 @@ struct FwdCfg {
   static_assert(NG == 2 || NG == 4, "two or four activation groups");
   // two groups come with a separate epilogue warpgroup; four fold the epilogue into the groups
   static constexpr bool SEP_EPI = NG == 2;
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES;
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - EXTRA_BYTES - SF_RESERVE;
   // Q double-buffered when two K and two V stages still fit, else single
   static constexpr int QST = AVAIL - 2 * Q_BYTES >= 2 * (K_BYTES + V_BYTES) ? 2 : 1;
   static_assert(QST <= 4, "at most four Q slots");
@@ -96,8 +104,10 @@ struct FwdCfg {
   // where that still fits beside the rings.
   static constexpr int STAGE_BYTES =
       SEP_EPI && QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + 16384 <= AVAIL ? 16384 : 0;
+  // scale-factor atoms in shared memory: Q slots, K stages, V stages, then the constant P atom
+  static constexpr int SF_BYTES = MX ? (QST + KST) * NQB * SF_ATOM + VST * SF_ATOM + SF_ATOM : 0;
   static constexpr int SMEM_BYTES =
-      1024 + QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + STAGE_BYTES + EXTRA_BYTES;
+      1024 + QST * Q_BYTES + KST * K_BYTES + VST * V_BYTES + STAGE_BYTES + SF_BYTES + EXTRA_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "tiles do not fit in shared memory");
   static constexpr int K_STEP = ESZ == 1 ? 32 : 16;  // K of one MMA instruction
   static_assert(DQK % K_STEP == 0, "head dim must be a multiple of the MMA K step");
@@ -116,6 +126,10 @@ struct FwdCfg {
   // else the widest that divides the slice and its column offset
   static constexpr int OCH = NG == 4 ? 8 : (OCOLS % 32 == 0 ? 32 : (OCOLS % 16 == 0 ? 16 : 8));
   static constexpr uint32_t T_S = 0, T_P = 256, T_O = 384;  // TMEM column bases
+  // MX scale factors in the TMEM columns that e4m3 P leaves free ([288, 320)
+  // and [352, 384)): 4 columns per atom
+  static constexpr uint32_t T_SFQ = 288, T_SFP = T_SFQ + QST * NQB * 4, T_SFV = T_SFP + 4, T_SFK = 352;
+  static_assert(!MX || (T_SFV + VST * 4 <= 320 && T_SFK + KST * NQB * 4 <= 384), "MX scale factors do not fit in TMEM");
 };
 
 struct FwdItem {
@@ -385,6 +399,71 @@ __device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint
 #undef GDPA_ACT_CASE
 }
 
+// ---------------------------------------------------------------- MXFP8 scale factors
+
+// Scale-factor atoms (512 bytes, what tcgen05.cp copies to TMEM): atom row l,
+// word j, byte b holds the scale of tile row (Q, K) or value column (V)
+// l + 32 j and K block 4 g + b of atom g. The MMA warps load a step's scales
+// into registers (lane l: rows l + 32 j) one step ahead, store the atoms
+// into the step's shared-memory slot when they issue its MMAs, and copy them
+// to TMEM in order with those MMAs. Rows past the sequence, and V's key
+// blocks past it, take scale 2^0 (byte 127).
+template <class C>
+struct MxRowWords {
+  uint32_t w[4][C::NQB];
+};
+
+// E8M0 bytes of `nrows` tile rows (tokens t0 + r, head `head` of `heads`),
+// d_qk / 32 per row, read two at a time.
+template <class C>
+__device__ __forceinline__ void mx_row_words(MxRowWords<C>& out, const uint8_t* sf, int t0, int nrows, int heads,
+                                             int head, int lane) {
+  constexpr int NKB = C::DQK / 32;
+  static_assert(NKB % 2 == 0, "scale rows are read two bytes at a time");
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int r = lane + 32 * jj;
+#pragma unroll
+    for (int g = 0; g < C::NQB; ++g) out.w[jj][g] = 0x7F7F7F7Fu;
+    if (r < nrows) {
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(sf + (static_cast<size_t>(t0 + r) * heads + head) * NKB);
+#pragma unroll
+      for (int kb = 0; kb < NKB; kb += 2) {
+        const uint32_t sh = 8 * (kb % 4);
+        out.w[jj][kb / 4] = (out.w[jj][kb / 4] & ~(0xFFFFu << sh)) | (static_cast<uint32_t>(__ldg(src + kb / 2)) << sh);
+      }
+    }
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void mx_put_rows(uint8_t* atoms, const MxRowWords<C>& in, int lane) {
+#pragma unroll
+  for (int g = 0; g < C::NQB; ++g)
+    *reinterpret_cast<uint4*>(atoms + g * C::SF_ATOM + lane * 16) =
+        make_uint4(in.w[0][g], in.w[1][g], in.w[2][g], in.w[3][g]);
+}
+
+// V's scales for the step's 128 keys (4 blocks of 32) and value columns lane + 32 j.
+template <class C>
+__device__ __forceinline__ uint4 mx_v_words(const FwdArgs& a, const FwdItem& it, int kr0, int lane) {
+  const int blk0 = (it.k_start + kr0) / 32;
+  uint32_t w[4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    w[jj] = 0;
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      const uint32_t byte =
+          kr0 + 32 * kb < it.lk
+              ? __ldg(a.sf_v + (static_cast<size_t>(blk0 + kb) * a.pb.h_kv + it.g) * C::DV + lane + 32 * jj)
+              : 0x7Fu;
+      w[jj] |= byte << (8 * kb);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <class C>
@@ -397,7 +476,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* sK = sQ + C::QST * C::Q_BYTES;
   uint8_t* sV = sK + C::KST * C::K_BYTES;
   uint8_t* sStage = sV + C::VST * C::V_BYTES;  // STAGE_BYTES (may be 0)
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(sStage + C::STAGE_BYTES);
+  uint8_t* sSFQ = sStage + C::STAGE_BYTES;      // MX scale-factor atoms (SF_BYTES, may be 0)
+  uint8_t* sSFK = sSFQ + C::QST * C::NQB * C::SF_ATOM;
+  uint8_t* sSFV = sSFK + C::KST * C::NQB * C::SF_ATOM;
+  uint8_t* sSFP = sSFV + C::VST * C::SF_ATOM;
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(sStage + C::STAGE_BYTES + C::SF_BYTES);
   static_assert(sizeof(FwdSmem) <= 1024, "barrier block too large");
   static_assert(!C::SOFTMAX || 1024 + sizeof(FwdSoftmaxSmem) <= C::EXTRA_BYTES, "softmax block too large");
   // only softmax configurations reserve room for it
@@ -412,8 +495,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
+    constexpr uint32_t kFullCount = 1;
     for (int i = 0; i < C::QST; ++i) {
-      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_full[i], kFullCount);
       mbar_init(&sm.q_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -421,7 +505,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sm.p_full[i], 128 * C::NG);
     }
     for (int i = 0; i < C::KST; ++i) {
-      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_full[i], kFullCount);
       mbar_init(&sm.k_empty[i], 1);
     }
     for (int i = 0; i < C::VST; ++i) {
@@ -450,6 +534,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     prefetch_tmap(&tm_k);
   }
   if (warp == 3 && lane == 0) prefetch_tmap(&tm_v);
+  if constexpr (C::MX) {
+    if (warp == 3) {  // P's scale factors: 2^0 for every row and K block
+      for (int i = lane; i < C::SF_ATOM / 4; i += 32) reinterpret_cast<uint32_t*>(sSFP)[i] = 0x7F7F7F7Fu;
+      fence_async_shared();
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -543,6 +633,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       StepCursor sc;
       sc.start(args, n_work);
       bool ok = true;
+      // MX: the Q (item start) and K scale words of the step about to be issued; the next
+      // step's are loaded right after this step's MMAs (after its proxy fence, which would
+      // otherwise wait for them), so they arrive while the next step waits for its operands
+      MxRowWords<C> q_cur, k_cur;
+      auto load_qk = [&](const StepCursor& c, MxRowWords<C>& qw, MxRowWords<C>& kw) {
+        if constexpr (C::MX) {
+          if (c.j == c.it.lo) mx_row_words<C>(qw, args.sf_q, c.it.q_start + c.it.r0, c.it.rows, pb.h_q, c.it.h, lane);
+          mx_row_words<C>(kw, args.sf_k, c.it.k_start + c.j * kTileK, min(kTileK, c.it.lk - c.j * kTileK), pb.h_kv,
+                          c.it.g, lane);
+        }
+      };
+      if (sc.active) load_qk(sc, q_cur, k_cur);
       while (sc.active && ok) {
         const int slot = sc.item_idx % C::QST;
         const int b = u & 1;
@@ -558,10 +660,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         const uint64_t a0 = sdesc_at(dq0, slot * C::Q_BYTES), b0 = sdesc_at(dk0, ks * C::K_BYTES);
         const uint32_t d = tbase + C::T_S + b * 128;
+        // MX: this Q tile's (first step of its item) and this K stage's scale atoms into TMEM
+        const uint32_t sfq = tbase + C::T_SFQ + slot * C::NQB * 4, sfk = tbase + C::T_SFK + ks * C::NQB * 4;
+        if constexpr (C::MX) {
+          if (sc.j == sc.it.lo) {
+            mx_put_rows<C>(sSFQ + slot * C::NQB * C::SF_ATOM, q_cur, lane);
+            // V's 32-key scale blocks are counted from key 0 of the packed keys: a sequence must start on one
+            if (lane == 0 && sc.it.k_start % 32 != 0) atomicExch(args.status, 1);
+          }
+          mx_put_rows<C>(sSFK + ks * C::NQB * C::SF_ATOM, k_cur, lane);
+          fence_async_shared();
+          __syncwarp();
+          if (sc.j == sc.it.lo)
+            for (int g = 0; g < C::NQB; ++g)
+              tmem_cp_atom_w(sfq + g * 4, sdesc_rows16(smem_u32(sSFQ + (slot * C::NQB + g) * C::SF_ATOM)));
+          for (int g = 0; g < C::NQB; ++g)
+            tmem_cp_atom_w(sfk + g * 4, sdesc_rows16(smem_u32(sSFK + (ks * C::NQB + g) * C::SF_ATOM)));
+        }
 #pragma unroll
         for (int k = 0; k < C::S_MMAS; ++k) {
           const uint32_t off = (k / 4) * C::BOX_BYTES + (k % 4) * 32;
-          if constexpr (C::DT == DT_E4M3)
+          if constexpr (C::MX)  // one MMA per 32-element scale block k: atom k / 4, byte k % 4
+            mma_mx_ss_w(d, sdesc_at(a0, off), sdesc_at(b0, off), idesc_mx(128, 128, 0, 0, k % 4, k % 4),
+                        sfq + (k / 4) * 4, sfk + (k / 4) * 4, k > 0);
+          else if constexpr (C::DT == DT_E4M3)
             mma_f8_ss_w(d, sdesc_at(a0, off), sdesc_at(b0, off), C::IDESC_S, k > 0);
           else
             mma_f16_ss_w(d, sdesc_at(a0, off), sdesc_at(b0, off), C::IDESC_S, k > 0);
@@ -572,6 +694,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (sc.j == sc.it.hi) mma_commit_w(&sm.q_empty[slot]);
         ++u;
         sc.advance(args, n_work);
+        if (C::MX && sc.active) load_qk(sc, q_cur, k_cur);
       }
       if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
         mma_commit_w(&sm.drain[0]);
@@ -587,6 +710,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       StepCursor pc;
       pc.start(args, n_work);
       bool ok = true;
+      if constexpr (C::MX) tmem_cp_atom_w(tbase + C::T_SFP, sdesc_rows16(smem_u32(sSFP)));  // P: scale 1 throughout
+      // MX: V scale words of the step about to be issued (the next step's are loaded after its MMAs)
+      uint4 v_cur = make_uint4(0, 0, 0, 0);
+      if (C::MX && pc.active) v_cur = mx_v_words<C>(args, pc.it, pc.j * kTileK, lane);
       while (pc.active && ok) {
         const int b = u & 1;
         ok = mbar_wait(&sm.p_full[b], (u >> 1) & 1, abort_flag);
@@ -597,11 +724,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         const uint64_t b0 = sdesc_at(dv0, vs * C::V_BYTES);
         const bool acc = pc.j > pc.it.lo;
+        const uint32_t sfv = tbase + C::T_SFV + vs * 4;
+        if constexpr (C::MX) {
+          *reinterpret_cast<uint4*>(sSFV + vs * C::SF_ATOM + lane * 16) = v_cur;
+          fence_async_shared();
+          __syncwarp();
+          tmem_cp_atom_w(sfv, sdesc_rows16(smem_u32(sSFV + vs * C::SF_ATOM)));
+        }
 #pragma unroll
         for (int k = 0; k < C::PV_MMAS; ++k) {
           const uint32_t a_t = tbase + C::T_P + b * 64 + k * (C::K_STEP * C::ESZ / 4);
           const uint64_t bd = sdesc_at(b0, k * C::K_STEP * 128);
-          if constexpr (C::DT == DT_E4M3)
+          if constexpr (C::MX)  // K block k of 32 keys: byte k of the P and V atoms
+            mma_mx_ts_w(tbase + C::T_O, a_t, bd, idesc_mx(128, C::DV, 0, 1, k, k), tbase + C::T_SFP, sfv,
+                        (acc || k > 0) ? 1u : 0u);
+          else if constexpr (C::DT == DT_E4M3)
             mma_f8_ts_w(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
           else
             mma_f16_ts_w(tbase + C::T_O, a_t, bd, C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
@@ -612,6 +749,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (pc.j == pc.it.hi) mma_commit_w(&sm.o_full);
         ++u;
         pc.advance(args, n_work);
+        if (C::MX && pc.active) v_cur = mx_v_words<C>(args, pc.it, pc.j * kTileK, lane);
       }
       if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
         mma_commit_w(&sm.drain[1]);
@@ -983,14 +1121,26 @@ __host__ __device__ constexpr bool fwd_four_groups(int act, int dt) {
   return dt != DT_E4M3 ? (act == ACT_GELU || act == ACT_GELU_TANH || act == ACT_SILU) : kFp8FourGroups && act != ACT_SOFTMAX;
 }
 
-template <int DQK, int DV, int DT, int NG, bool SOFTMAX = false>
+template <int DQK, int DV, int DT, int NG, bool SOFTMAX = false, bool MX = false>
 cudaError_t launch_fwd_ng(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                           int grid, cudaStream_t stream) {
-  using C = FwdCfg<DQK, DV, DT, NG, SOFTMAX>;
+  using C = FwdCfg<DQK, DV, DT, NG, SOFTMAX, MX>;
   auto kern = gdpa_fwd_kernel<C>;
   const cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, tq, tk, tv, a);
+}
+
+// MXFP8 (block-scaled e4m3): head dims with d_v = 128 only.
+template <int DQK, int DV>
+cudaError_t launch_fwd_mx(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                          int grid, cudaStream_t stream) {
+  if constexpr (DV == 128 && DQK % 32 == 0) {
+    if (a.act == ACT_SOFTMAX) return launch_fwd_ng<DQK, DV, DT_E4M3, 2, true, true>(tq, tk, tv, a, grid, stream);
+    return launch_fwd_ng<DQK, DV, DT_E4M3, 2, false, true>(tq, tk, tv, a, grid, stream);
+  } else {
+    return cudaErrorNotSupported;
+  }
 }
 
 template <int DQK, int DV, int DT>

@@ -320,6 +320,66 @@ __device__ __forceinline__ void mma_f8_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled e4m3 (kind::mxf8f6f4, one E8M0 scale per 32 K elements of
+// each row of A and of B). sfa / sfb: TMEM addresses of the scale factors;
+// the instruction descriptor's A / B scale-factor ids pick the byte of each
+// 32-bit TMEM word (see idesc_mx). A from shared memory (ss) or TMEM (ts).
+__device__ __forceinline__ void mma_mx_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, e;\n"
+      " setp.ne.b32 p, %6, 0;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mx_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, e;\n"
+      " setp.ne.b32 p, %6, 0;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], [%1], %2, %3, [%4], [%5], p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Copies one 512-byte scale-factor atom from shared memory to TMEM columns
+// [taddr, taddr + 4) of every lane quadrant: atom row l (16 bytes) goes to
+// lane l of each quadrant. Issued by one elected lane, in order with the
+// same thread's MMAs.
+__device__ __forceinline__ void tmem_cp_atom_w(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n"
+      " .reg .pred e;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n"
+      "}\n" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+// Shared-memory descriptor of a no-swizzle source of 16-byte rows (8-row
+// core matrices 128 bytes apart), as tcgen05.cp reads a scale-factor atom.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version (tcgen05); layout 0: no swizzle
+  return d;
+}
+// Instruction descriptor of kind::mxf8f6f4 with e4m3 A and B and E8M0 scales:
+// the kind::f8f6f4 fields, plus the B scale-factor id in bits [4, 6), the
+// scale type (1 = E8M0) in bit 23 and the A scale-factor id in bits [29, 31).
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t m, uint32_t n, uint32_t a_mn, uint32_t b_mn, uint32_t a_sf,
+                                                uint32_t b_sf) {
+  return (b_sf << 4) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (a_sf << 29);
+}
+
 // Warp-wide commit (one elected lane).
 __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
   asm volatile(

@@ -129,6 +129,31 @@ int gdpa_fwd(const gdpa_shape* shape, const void* q, const void* k, const void* 
              const float* descale_qkv, void* out, float* lse, void* workspace,
              size_t workspace_bytes, void* stream);
 
+/* MXFP8 forward ("MXFP8 forward" is listed as coming soon on the gdpa/README.md
+ * page, "Features", Datatypes; the block-scale layout is not on the page and
+ * follows the OCP Microscaling (MX) v1.0 format: blocks of 32 elements share
+ * one E8M0 scale byte s, element value = e4m3 code * 2^(s - 127), s = 255
+ * being NaN). q, k, v hold e4m3 codes (shape->dtype = GDPA_E4M3) in the
+ * layouts above; out is bf16. The blocks run along the contraction of each
+ * GEMM:
+ *   q_scale [total_q, h_q, d_qk / 32]: block i of q[t, h, :] is elements 32i..32i+31;
+ *   k_scale [total_k, h_kv, d_qk / 32]: likewise for k;
+ *   v_scale [ceil(total_k / 32), h_kv, d_v]: block j of column v[:, g, n] is
+ *     packed key tokens 32j..32j+31, so every key sequence must start at a
+ *     multiple of 32 (cu_seqlens_k[b] % 32 == 0; without cu_seqlens,
+ *     max_seqlen_k % 32 == 0, checked on the host). A sequence that does not
+ *     records GDPA_ERR_INVALID in the status word (its rows are then wrong).
+ *     Keys past a sequence's end inside its last block are ignored.
+ * The MMAs apply the scales (tcgen05 kind::mxf8f6f4); P is quantised to e4m3
+ * with scale 2^0. Head dims (128, 128) and (192, 128); every activation,
+ * softmax included. The scale pointers must be 16-byte aligned. Other
+ * arguments and errors as for gdpa_fwd (descale is not used). */
+int gdpa_fwd_mxfp8(const gdpa_shape* shape, const void* q, const void* k, const void* v,
+                   const uint8_t* q_scale, const uint8_t* k_scale, const uint8_t* v_scale,
+                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+                   int max_seqlen_k, int act, float scale, int causal, int window, void* out,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Backward (bf16/fp16 only). Arguments as for gdpa_fwd; out and lse are read
  * only for GDPA_ACT_SOFTMAX (they must be the forward's results) and may be
  * NULL otherwise. dout has out's layout; dq, dk, dv have q's, k's and v's.

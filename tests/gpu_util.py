@@ -33,6 +33,7 @@ def to_dev(inp):
     d["cu_q"] = None if fixed else inp.cu_seqlens_q.cuda()
     d["cu_k"] = None if fixed else inp.cu_seqlens_k.cuda()
     d["descale"] = None if inp.descale is None else torch.tensor(inp.descale, dtype=torch.float32).cuda()
+    d["mx"] = None if inp.mx is None else tuple(t.cuda() for t in inp.mx)
     return d
 
 
@@ -47,8 +48,12 @@ def run_fwd(inp, act=None):
     wl = inp.wl
     d = to_dev(inp)
     mq, mk = max_lens(inp)
-    out, lse = _lib.gdpa_fwd(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"], mq, mk, act or wl.act,
-                             wl.softmax_scale, wl.causal, wl.window, descale_qkv=d["descale"], batch=wl.batch)
+    if d["mx"] is not None:
+        out, lse = _lib.gdpa_fwd_mxfp8(d["q"], d["k"], d["v"], *d["mx"], d["cu_q"], d["cu_k"], mq, mk, act or wl.act,
+                                       wl.softmax_scale, wl.causal, wl.window, batch=wl.batch)
+    else:
+        out, lse = _lib.gdpa_fwd(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"], mq, mk, act or wl.act,
+                                 wl.softmax_scale, wl.causal, wl.window, descale_qkv=d["descale"], batch=wl.batch)
     assert _lib.gdpa_get_status() == 0
     return out, lse
 

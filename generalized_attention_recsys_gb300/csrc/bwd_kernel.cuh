@@ -317,7 +317,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const Problem& pb = args.pb;
-  const int n_work = args.work->count * pb.h_kv * C::NPART;
   const int G = gridDim.x;
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -359,6 +358,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
   pdl_wait();  // the work list, the cleared accumulator and the inputs come from earlier kernels
+  // read only after the wait: the work list is the previous kernel's output
+  const int n_work = args.work->count * pb.h_kv * C::NPART;
   pdl_release();
   // registers: control warpgroup 96, elementwise warpgroups 160, drain warpgroup 96
   // (128 * 96 + 256 * 160 + 128 * 96 = 65536 = 512 * 128 launched)

@@ -489,7 +489,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const Problem& pb = args.pb;
-  const int n_work = args.work->count * pb.h_q;
   volatile int* abort_flag = &sm.abort_flag;
   constexpr bool softmax = C::SOFTMAX;
 
@@ -545,6 +544,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
   pdl_wait();  // the work list and inputs come from earlier kernels; out may still be read
+  // read only after the wait: the work list is the previous kernel's output
+  const int n_work = args.work->count * pb.h_q;
   pdl_release();
 
   if (warp == 0) {

@@ -116,7 +116,7 @@ def make_shape(q, k, v, batch: int) -> GdpaShape:
 
 
 def gdpa_workspace_bytes(shape: GdpaShape, max_seqlen_q: int, max_seqlen_k: int, is_bwd: int) -> int:
-    """is_bwd: 0 forward, 1 backward, 2 deterministic backward (C-ABI gdpa_workspace_bytes)."""
+    """is_bwd: 0 forward, 1 backward, 2 deterministic backward, 3 MXFP8 forward (C-ABI gdpa_workspace_bytes)."""
     return int(load().gdpa_workspace_bytes(ctypes.byref(shape), max_seqlen_q, max_seqlen_k, int(is_bwd)))
 
 
@@ -169,7 +169,7 @@ def gdpa_fwd_mxfp8(q, k, v, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlens_
     for t in (q_scale, k_scale, v_scale):
         if t is not None and t.dtype != torch.uint8:
             raise TypeError("MX scales are E8M0 bytes (torch.uint8)")
-    nb = gdpa_workspace_bytes(shape, max_seqlen_q, max_seqlen_k, False)
+    nb = gdpa_workspace_bytes(shape, max_seqlen_q, max_seqlen_k, 3)
     ws = _workspace(nb, q.device, workspace)
     st = lib.gdpa_fwd_mxfp8(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale),
                             _ptr(v_scale), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q),

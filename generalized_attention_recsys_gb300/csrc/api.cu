@@ -133,6 +133,15 @@ size_t bwd_list_cap(const gdpa_shape* s) {
 }
 size_t list_bytes(size_t cap) { return round256(offsetof(WorkList, items) + sizeof(WorkEntry) * cap); }
 
+// MXFP8 forward: the scale atoms (512 bytes each; see mx_stage_atoms), per work item and
+// 4-block group of q, per 32-key group and kv head for k (4-block groups) and v.
+constexpr size_t kAtom = 512;
+size_t mx_nqb(const gdpa_shape* s) { return (static_cast<size_t>(s->d_qk) / 32 + 3) / 4; }
+size_t mx_groups(const gdpa_shape* s) { return (static_cast<size_t>(s->total_k) + 31) / 32; }
+size_t mx_q_atom_bytes(const gdpa_shape* s) { return round256(fwd_list_cap(s) * s->h_q * mx_nqb(s) * kAtom); }
+size_t mx_k_atom_bytes(const gdpa_shape* s) { return round256(mx_groups(s) * s->h_kv * mx_nqb(s) * kAtom); }
+size_t mx_v_atom_bytes(const gdpa_shape* s) { return round256(mx_groups(s) * s->h_kv * kAtom); }
+
 // Deterministic backward: one fp32 dQ slice [total_q, h_q, d_qk] per key block.
 size_t dq_part_bytes(const gdpa_shape* s, int max_k) {
   const size_t nkv = max_k > 0 ? (static_cast<size_t>(max_k) + kTileK - 1) / kTileK : 0;
@@ -270,6 +279,182 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
   }
 }
 
+// MXFP8: rearranges the caller's E8M0 scales into the atoms that tcgen05.cp
+// copies to TMEM (row l, word j, byte b: tile row or value column l + 32 j,
+// K block 4 g + b of atom g), so that the forward's producers load them with
+// plain bulk copies.
+//   q: per work item (entry e, head h: position e h_q + h) and atom g, rows
+//      q_start + r0 + r of the item's tile (past its rows: 2^0);
+//   k: per 32-key group G and kv head, and atom g: keys 32 G + r (the 128-key
+//      tile that starts at G; past total_k: 2^0);
+//   v: per 32-key group G and kv head: value column n, the four 32-key blocks
+//      G..G+3 of the tile that starts at G.
+// q and k go through shared memory a tile of rows at a time (a work entry's
+// 128 rows, or the rows of up to 8 consecutive key groups), read in 16-byte
+// chunks; one thread then writes one 16-byte atom row. The tile's row stride
+// is an odd number of words, so the 32 rows a warp reads fall in 32 banks.
+// Also checks that every key sequence starts on a 32-key block (V's blocks
+// are counted from key 0): one that does not is reported as GDPA_ERR_INVALID.
+constexpr int kStageSmem = 48 * 1024 - 16;        // tile bytes (mx_stage_atoms takes 48 KB: 16 for the read past the end)
+constexpr int kStageRowWords = kStageSmem / 512;  // >= row stride (words) of a 128-row tile
+
+// Odd number of words that holds a tile row of w bytes.
+__device__ __forceinline__ int stage_stride(int w) { return ((w + 3) / 4) | 1; }
+
+// Copies bytes [c0, c0 + w) of rows t0 .. t0 + n - 1 (n >= 1) of the row-major
+// byte matrix src (rows of rl bytes, nbytes in all, 16-byte aligned) into
+// tile rows 0 .. n - 1 (stride words apart), reading 16-byte chunks. With rl,
+// c0 and w multiples of 4 it moves words, else bytes (E = 4 or 1 bytes).
+template <typename E>
+__device__ __forceinline__ void stage_rows_as(const uint8_t* src, size_t nbytes, int rl, int t0, int n, int c0, int w,
+                                              uint32_t* tile, int stride) {
+  constexpr int S = sizeof(E), PER = 16 / S;  // elements per chunk
+  const E* se = reinterpret_cast<const E*>(src);
+  E* te = reinterpret_cast<E*>(tile);
+  const int rle = rl / S, c0e = c0 / S, we = w / S, se_stride = stride * 4 / S;
+  const size_t ne = nbytes / S;  // whole elements in src (nbytes is a multiple of S)
+  const size_t first = static_cast<size_t>(t0) * rle;
+  const size_t lo = first + c0e, hi = first + static_cast<size_t>(n - 1) * rle + c0e + we;
+  const size_t base = lo & ~static_cast<size_t>(PER - 1);
+  const int nchunks = static_cast<int>((hi - base + PER - 1) / PER);
+  const int rel0 = static_cast<int>(static_cast<long long>(base) - static_cast<long long>(first));  // >= -(PER - 1)
+  constexpr int U = 4;
+  for (int c = threadIdx.x; c < nchunks; c += U * blockDim.x) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cu = c + u * blockDim.x;
+      const size_t o = base + static_cast<size_t>(cu) * PER;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (cu < nchunks) {
+        if (o + PER <= ne) {
+          v[u] = __ldg(reinterpret_cast<const uint4*>(se + o));
+        } else {
+          E* ve = reinterpret_cast<E*>(&v[u]);
+          for (int k = 0; k < PER && o + k < ne; ++k) ve[k] = se[o + k];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cu = c + u * blockDim.x;
+      if (cu >= nchunks) break;
+      const E* ve = reinterpret_cast<const E*>(&v[u]);
+      const int rel = rel0 + cu * PER;  // element offset from row t0's start
+      int r = rel >= 0 ? rel / rle : -((-rel + rle - 1) / rle);
+      int col = rel - r * rle;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        if (r >= 0 && r < n && col >= c0e && col < c0e + we) te[r * se_stride + col - c0e] = ve[k];
+        if (++col == rle) {
+          col = 0;
+          ++r;
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) mx_stage_atoms(Problem pb, const WorkList* wl, int nqb, int nkb, int dv,
+                                                      const uint8_t* sf_q, const uint8_t* sf_k, const uint8_t* sf_v,
+                                                      uint4* aq, uint4* ak, uint4* av, int* status) {
+  extern __shared__ uint4 stage_smem[];  // kStageSmem bytes of tile, plus one word read past its end
+  uint32_t* tile = reinterpret_cast<uint32_t*>(stage_smem);
+  pdl_wait();  // the work list is the previous kernel's
+  pdl_release();
+  const int ngroups = (pb.total_k + 31) / 32;
+  const int max_heads = (kStageRowWords - 1) * 4 / nkb;  // heads whose row fits an odd stride <= kStageRowWords
+  const int hcq = min(pb.h_q, max_heads), hck = min(pb.h_kv, max_heads);
+  const int cq = (pb.h_q + hcq - 1) / hcq, ck = (pb.h_kv + hck - 1) / hck;
+  const int sk = stage_stride(hck * nkb);
+  const int ngk = max(1, min(8, (kStageSmem / (4 * sk) - 96) / 32));  // key groups per k tile
+  const int n_qu = wl->count * cq, n_ku = (ngroups + ngk - 1) / ngk * ck;
+  for (int u = blockIdx.x; u < n_qu + n_ku; u += gridDim.x) {
+    int h0, hc, heads, t0, nvalid, ng, atom0;  // atom0: the unit's first atom (for its first group and head h0)
+    const uint8_t* src;
+    size_t nbytes;
+    uint4* dst;
+    if (u < n_qu) {  // work entry e, heads h0 ..
+      const int e = u / cq;
+      h0 = (u - e * cq) * hcq;
+      hc = min(hcq, pb.h_q - h0);
+      heads = pb.h_q;
+      t0 = wl->items[e].seq.x + wl->items[e].blk.x;
+      nvalid = wl->items[e].blk.y;
+      ng = 1;
+      atom0 = (e * heads + h0) * nqb;
+      src = sf_q;
+      nbytes = static_cast<size_t>(pb.total_q) * pb.h_q * nkb;
+      dst = aq;
+    } else {  // key groups G0 .. G0 + ng - 1, kv heads h0 ..
+      const int v = u - n_qu, gc = v / ck, g0 = gc * ngk;
+      h0 = (v - gc * ck) * hck;
+      hc = min(hck, pb.h_kv - h0);
+      heads = pb.h_kv;
+      t0 = 32 * g0;
+      ng = min(ngk, ngroups - g0);
+      nvalid = min(32 * ng + 96, pb.total_k - t0);
+      atom0 = (g0 * heads + h0) * nqb;
+      src = sf_k;
+      nbytes = static_cast<size_t>(pb.total_k) * pb.h_kv * nkb;
+      dst = ak;
+    }
+    const int w = hc * nkb, stride = stage_stride(w), rl = heads * nkb, c0 = h0 * nkb;
+    __syncthreads();  // the previous tile's reads are done
+    if (nvalid > 0) {
+      if (((rl | c0 | w) & 3) == 0)
+        stage_rows_as<uint32_t>(src, nbytes, rl, t0, nvalid, c0, w, tile, stride);
+      else
+        stage_rows_as<uint8_t>(src, nbytes, rl, t0, nvalid, c0, w, tile, stride);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < ng * hc * nqb * 32; i += blockDim.x) {  // one atom row each
+      const int a = i >> 5, l = i & 31;
+      const int gi = a / (hc * nqb), rem = a - gi * hc * nqb;
+      const int hh = rem / nqb, g = rem - hh * nqb;
+      const int ob = hh * nkb + 4 * g, ow = ob >> 2, sh = (ob & 3) * 8;  // the atom's bytes in a tile row
+      const int nb = min(4, nkb - 4 * g);                                 // K blocks present (rest: 2^0)
+      const uint32_t keep = nb == 4 ? 0xFFFFFFFFu : (1u << (8 * nb)) - 1;
+      uint32_t wd[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = 32 * gi + l + 32 * j;
+        wd[j] = 0x7F7F7F7Fu;
+        if (r < nvalid) {
+          const uint32_t* row = tile + r * stride + ow;
+          const uint32_t x = sh ? __funnelshift_r(row[0], row[1], sh) : row[0];
+          wd[j] = (x & keep) | (0x7F7F7F7Fu & ~keep);
+        }
+      }
+      dst[(static_cast<size_t>(atom0) + static_cast<size_t>(gi) * heads * nqb + rem) * 32 + l] =
+          make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+  }
+  const int n_vr = ngroups * pb.h_kv * 32;  // v atom rows
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_vr; i += gridDim.x * blockDim.x) {
+    const int a = i >> 5, l = i & 31;
+    const int grp = a / pb.h_kv, head = a - grp * pb.h_kv;
+    uint32_t wd[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      wd[j] = 0x7F7F7F7Fu;
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (grp + b < ngroups)
+          wd[j] = (wd[j] & ~(0xFFu << (8 * b))) |
+                  (static_cast<uint32_t>(sf_v[(static_cast<size_t>(grp + b) * pb.h_kv + head) * dv + l + 32 * j])
+                   << (8 * b));
+    }
+    av[i] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  }
+  if (blockIdx.x == 0)
+    for (int b = threadIdx.x; b < pb.batch; b += blockDim.x) {
+      int ks, lk;
+      seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
+      if (ks % 32 != 0) atomicExch(status, 1);
+    }
+}
+
 thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
 
 #ifdef GDPA_TEST_HOOKS
@@ -309,6 +494,8 @@ extern "C" {
 size_t gdpa_workspace_bytes(const gdpa_shape* s, int max_q, int max_k, int is_bwd) {
   if (validate(s, max_q, max_k, GDPA_ACT_IDENTITY, 0, 0) != GDPA_OK) return 0;
   if (!is_bwd) return list_bytes(fwd_list_cap(s));
+  if (is_bwd == 3)  // gdpa_fwd_mxfp8: the forward's list and the scale atoms
+    return list_bytes(fwd_list_cap(s)) + mx_q_atom_bytes(s) + mx_k_atom_bytes(s) + mx_v_atom_bytes(s);
   size_t b = list_bytes(bwd_list_cap(s));
   b += round256(static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float));  // dQ accumulator
   b += round256(static_cast<size_t>(s->total_q) * s->h_q * sizeof(float));            // softmax rowsum(dO*O)
@@ -342,7 +529,7 @@ int fwd_common(const gdpa_shape* s, const void* q, const void* k, const void* v,
   if (!cu_q && (s->total_q != s->batch * max_q || s->total_k != s->batch * max_k)) return GDPA_ERR_INVALID;
   if (act == GDPA_ACT_SOFTMAX && !lse) return GDPA_ERR_INVALID;
   if (s->dtype == GDPA_E4M3 && !descale && !mx) return GDPA_ERR_INVALID;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, 0))
+  if (!workspace || !aligned16(workspace) || workspace_bytes < gdpa_workspace_bytes(s, max_q, max_k, mx ? 3 : 0))
     return GDPA_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const int nsm = sm_count();
@@ -355,6 +542,17 @@ int fwd_common(const gdpa_shape* s, const void* q, const void* k, const void* v,
   if (launch_pdl(build_worklist, dim3(1), dim3(1024), 0, stream, pb, 0, wl, cap, static_cast<float4*>(nullptr),
                  static_cast<size_t>(0)) != cudaSuccess)
     return GDPA_ERR_CUDA;
+  uint8_t *atoms_q = nullptr, *atoms_k = nullptr, *atoms_v = nullptr;
+  if (mx) {
+    atoms_q = static_cast<uint8_t*>(workspace) + list_bytes(fwd_list_cap(s));
+    atoms_k = atoms_q + mx_q_atom_bytes(s);
+    atoms_v = atoms_k + mx_k_atom_bytes(s);
+    if (launch_pdl(mx_stage_atoms, dim3(4 * nsm), dim3(256), kStageSmem + 16, stream, pb,
+                   static_cast<const WorkList*>(wl), static_cast<int>(mx_nqb(s)), s->d_qk / 32, s->d_v, sf_q, sf_k,
+                   sf_v, reinterpret_cast<uint4*>(atoms_q), reinterpret_cast<uint4*>(atoms_k),
+                   reinterpret_cast<uint4*>(atoms_v), status) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+  }
 
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, s->total_q, s->h_q, s->d_qk, s->dtype, workspace) ||
@@ -370,6 +568,9 @@ int fwd_common(const gdpa_shape* s, const void* q, const void* k, const void* v,
   a.sf_q = sf_q;
   a.sf_k = mx ? sf_k : nullptr;
   a.sf_v = mx ? sf_v : nullptr;
+  a.atoms_q = atoms_q;
+  a.atoms_k = atoms_k;
+  a.atoms_v = atoms_v;
   a.out = out;
   a.lse = lse;
   a.work = wl;

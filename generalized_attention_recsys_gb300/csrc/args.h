@@ -63,6 +63,12 @@ struct FwdArgs {
   const uint8_t* sf_q;
   const uint8_t* sf_k;
   const uint8_t* sf_v;
+  // MXFP8: the same scales rearranged into 512-byte TMEM-copy atoms (workspace, written by a
+  // kernel before the forward): per work item and 4-block group of q; per 32-key group (the
+  // tile of 128 keys starting there) and kv head for k (4-block groups) and for v
+  const uint8_t* atoms_q;
+  const uint8_t* atoms_k;
+  const uint8_t* atoms_v;
   void* out;             // [total_q, h_q, dv]; bf16 for bf16/e4m3 inputs, f16 for f16
   float* lse;            // [h_q, total_q] (softmax)
   const WorkList* work;

@@ -135,6 +135,7 @@ struct FwdCfg {
 struct FwdItem {
   int h, g, q_start, lq, k_start, lk;
   int r0, rows, lo, hi, n;
+  int pos;  // position in the work order (entry * h_q + head)
 };
 
 __device__ __forceinline__ FwdItem fwd_decode(const FwdArgs& a, int pos) {
@@ -153,6 +154,7 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdArgs& a, int pos) {
   it.lo = bk.z;
   it.n = bk.w;
   it.hi = it.lo + it.n - 1;
+  it.pos = pos;
   return it;
 }
 
@@ -400,69 +402,14 @@ __device__ __forceinline__ bool act_quarter_dispatch(int act, uint32_t t_s, uint
 }
 
 // ---------------------------------------------------------------- MXFP8 scale factors
-
+//
 // Scale-factor atoms (512 bytes, what tcgen05.cp copies to TMEM): atom row l,
 // word j, byte b holds the scale of tile row (Q, K) or value column (V)
-// l + 32 j and K block 4 g + b of atom g. The MMA warps load a step's scales
-// into registers (lane l: rows l + 32 j) one step ahead, store the atoms
-// into the step's shared-memory slot when they issue its MMAs, and copy them
-// to TMEM in order with those MMAs. Rows past the sequence, and V's key
-// blocks past it, take scale 2^0 (byte 127).
-template <class C>
-struct MxRowWords {
-  uint32_t w[4][C::NQB];
-};
-
-// E8M0 bytes of `nrows` tile rows (tokens t0 + r, head `head` of `heads`),
-// d_qk / 32 per row, read two at a time.
-template <class C>
-__device__ __forceinline__ void mx_row_words(MxRowWords<C>& out, const uint8_t* sf, int t0, int nrows, int heads,
-                                             int head, int lane) {
-  constexpr int NKB = C::DQK / 32;
-  static_assert(NKB % 2 == 0, "scale rows are read two bytes at a time");
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int r = lane + 32 * jj;
-#pragma unroll
-    for (int g = 0; g < C::NQB; ++g) out.w[jj][g] = 0x7F7F7F7Fu;
-    if (r < nrows) {
-      const uint16_t* src = reinterpret_cast<const uint16_t*>(sf + (static_cast<size_t>(t0 + r) * heads + head) * NKB);
-#pragma unroll
-      for (int kb = 0; kb < NKB; kb += 2) {
-        const uint32_t sh = 8 * (kb % 4);
-        out.w[jj][kb / 4] = (out.w[jj][kb / 4] & ~(0xFFFFu << sh)) | (static_cast<uint32_t>(__ldg(src + kb / 2)) << sh);
-      }
-    }
-  }
-}
-
-template <class C>
-__device__ __forceinline__ void mx_put_rows(uint8_t* atoms, const MxRowWords<C>& in, int lane) {
-#pragma unroll
-  for (int g = 0; g < C::NQB; ++g)
-    *reinterpret_cast<uint4*>(atoms + g * C::SF_ATOM + lane * 16) =
-        make_uint4(in.w[0][g], in.w[1][g], in.w[2][g], in.w[3][g]);
-}
-
-// V's scales for the step's 128 keys (4 blocks of 32) and value columns lane + 32 j.
-template <class C>
-__device__ __forceinline__ uint4 mx_v_words(const FwdArgs& a, const FwdItem& it, int kr0, int lane) {
-  const int blk0 = (it.k_start + kr0) / 32;
-  uint32_t w[4];
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    w[jj] = 0;
-#pragma unroll
-    for (int kb = 0; kb < 4; ++kb) {
-      const uint32_t byte =
-          kr0 + 32 * kb < it.lk
-              ? __ldg(a.sf_v + (static_cast<size_t>(blk0 + kb) * a.pb.h_kv + it.g) * C::DV + lane + 32 * jj)
-              : 0x7Fu;
-      w[jj] |= byte << (8 * kb);
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
+// l + 32 j and K block 4 g + b of atom g. A kernel before the forward writes
+// them into the workspace from the caller's E8M0 tensors (mx_stage_atoms);
+// the TMA producers bulk-copy each tile's atoms into its shared-memory slot
+// with the tile, completing on the same barrier, and the MMA warps copy them
+// to TMEM in order with the tile's MMAs.
 
 // ---------------------------------------------------------------- the kernel
 
@@ -562,10 +509,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int ks = k_it % C::KST;
         ok = mbar_wait(&sm.k_empty[ks], ((k_it / C::KST) & 1) ^ 1, abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(&sm.k_full[ks], C::K_BYTES);
+        mbar_arrive_expect_tx(&sm.k_full[ks], C::K_BYTES + (C::MX ? C::NQB * C::SF_ATOM : 0));
         for (int bx = 0; bx < C::QK_BOXES; ++bx)
           tma_load_3d(sK + ks * C::K_BYTES + bx * C::BOX_BYTES, &tm_k, &sm.k_full[ks], bx * C::BOX_ELEMS, kc.it.g,
                       kc.it.k_start + kc.j * kTileK);
+        if constexpr (C::MX) {  // the K tile's scale atoms (keyed by its first 32-key group)
+          const size_t grp = static_cast<size_t>((kc.it.k_start + kc.j * kTileK) / 32) * pb.h_kv + kc.it.g;
+          bulk_load_1d(sSFK + ks * C::NQB * C::SF_ATOM, args.atoms_k + grp * C::NQB * C::SF_ATOM,
+                       C::NQB * C::SF_ATOM, &sm.k_full[ks]);
+        }
         ++k_it;
         kc.advance(args, n_work);
       }
@@ -584,10 +536,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int slot = qc.item_idx % C::QST;
         ok = mbar_wait(&sm.q_empty[slot], ((qc.item_idx / C::QST) & 1) ^ 1, abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(&sm.q_full[slot], C::Q_BYTES);
+        mbar_arrive_expect_tx(&sm.q_full[slot], C::Q_BYTES + (C::MX ? C::NQB * C::SF_ATOM : 0));
         for (int bx = 0; bx < C::QK_BOXES; ++bx)
           tma_load_3d(sQ + slot * C::Q_BYTES + bx * C::BOX_BYTES, &tm_q, &sm.q_full[slot], bx * C::BOX_ELEMS,
                       qc.it.h, qc.it.q_start + qc.it.r0);
+        if constexpr (C::MX)  // the Q tile's scale atoms (keyed by the work item)
+          bulk_load_1d(sSFQ + slot * C::NQB * C::SF_ATOM,
+                       args.atoms_q + static_cast<size_t>(qc.it.pos) * C::NQB * C::SF_ATOM, C::NQB * C::SF_ATOM,
+                       &sm.q_full[slot]);
         ++q_loads;
         qc.next_item(args, n_work);
       }
@@ -611,10 +567,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int vs = v_it % C::VST;
         ok = mbar_wait(&sm.v_empty[vs], ((v_it / C::VST) & 1) ^ 1, abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(&sm.v_full[vs], C::V_BYTES);
+        mbar_arrive_expect_tx(&sm.v_full[vs], C::V_BYTES + (C::MX ? C::SF_ATOM : 0));
         for (int bx = 0; bx < C::V_BOXES; ++bx)
           tma_load_3d(sV + vs * C::V_BYTES + bx * C::BOX_BYTES, &tm_v, &sm.v_full[vs], bx * C::BOX_ELEMS, vc.it.g,
                       vc.it.k_start + vc.j * kTileK);
+        if constexpr (C::MX) {  // the V tile's scale atom
+          const size_t grp = static_cast<size_t>((vc.it.k_start + vc.j * kTileK) / 32) * pb.h_kv + vc.it.g;
+          bulk_load_1d(sSFV + vs * C::SF_ATOM, args.atoms_v + grp * C::SF_ATOM, C::SF_ATOM, &sm.v_full[vs]);
+        }
         ++v_it;
         vc.advance(args, n_work);
       }
@@ -634,18 +594,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       StepCursor sc;
       sc.start(args, n_work);
       bool ok = true;
-      // MX: the Q (item start) and K scale words of the step about to be issued; the next
-      // step's are loaded right after this step's MMAs (after its proxy fence, which would
-      // otherwise wait for them), so they arrive while the next step waits for its operands
-      MxRowWords<C> q_cur, k_cur;
-      auto load_qk = [&](const StepCursor& c, MxRowWords<C>& qw, MxRowWords<C>& kw) {
-        if constexpr (C::MX) {
-          if (c.j == c.it.lo) mx_row_words<C>(qw, args.sf_q, c.it.q_start + c.it.r0, c.it.rows, pb.h_q, c.it.h, lane);
-          mx_row_words<C>(kw, args.sf_k, c.it.k_start + c.j * kTileK, min(kTileK, c.it.lk - c.j * kTileK), pb.h_kv,
-                          c.it.g, lane);
-        }
-      };
-      if (sc.active) load_qk(sc, q_cur, k_cur);
       while (sc.active && ok) {
         const int slot = sc.item_idx % C::QST;
         const int b = u & 1;
@@ -662,16 +610,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint64_t a0 = sdesc_at(dq0, slot * C::Q_BYTES), b0 = sdesc_at(dk0, ks * C::K_BYTES);
         const uint32_t d = tbase + C::T_S + b * 128;
         // MX: this Q tile's (first step of its item) and this K stage's scale atoms into TMEM
+        // (the atoms came with the tiles, by bulk copy)
         const uint32_t sfq = tbase + C::T_SFQ + slot * C::NQB * 4, sfk = tbase + C::T_SFK + ks * C::NQB * 4;
         if constexpr (C::MX) {
-          if (sc.j == sc.it.lo) {
-            mx_put_rows<C>(sSFQ + slot * C::NQB * C::SF_ATOM, q_cur, lane);
-            // V's 32-key scale blocks are counted from key 0 of the packed keys: a sequence must start on one
-            if (lane == 0 && sc.it.k_start % 32 != 0) atomicExch(args.status, 1);
-          }
-          mx_put_rows<C>(sSFK + ks * C::NQB * C::SF_ATOM, k_cur, lane);
-          fence_async_shared();
-          __syncwarp();
           if (sc.j == sc.it.lo)
             for (int g = 0; g < C::NQB; ++g)
               tmem_cp_atom_w(sfq + g * 4, sdesc_rows16(smem_u32(sSFQ + (slot * C::NQB + g) * C::SF_ATOM)));
@@ -695,7 +636,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (sc.j == sc.it.hi) mma_commit_w(&sm.q_empty[slot]);
         ++u;
         sc.advance(args, n_work);
-        if (C::MX && sc.active) load_qk(sc, q_cur, k_cur);
       }
       if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
         mma_commit_w(&sm.drain[0]);
@@ -712,9 +652,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       pc.start(args, n_work);
       bool ok = true;
       if constexpr (C::MX) tmem_cp_atom_w(tbase + C::T_SFP, sdesc_rows16(smem_u32(sSFP)));  // P: scale 1 throughout
-      // MX: V scale words of the step about to be issued (the next step's are loaded after its MMAs)
-      uint4 v_cur = make_uint4(0, 0, 0, 0);
-      if (C::MX && pc.active) v_cur = mx_v_words<C>(args, pc.it, pc.j * kTileK, lane);
       while (pc.active && ok) {
         const int b = u & 1;
         ok = mbar_wait(&sm.p_full[b], (u >> 1) & 1, abort_flag);
@@ -726,12 +663,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint64_t b0 = sdesc_at(dv0, vs * C::V_BYTES);
         const bool acc = pc.j > pc.it.lo;
         const uint32_t sfv = tbase + C::T_SFV + vs * 4;
-        if constexpr (C::MX) {
-          *reinterpret_cast<uint4*>(sSFV + vs * C::SF_ATOM + lane * 16) = v_cur;
-          fence_async_shared();
-          __syncwarp();
-          tmem_cp_atom_w(sfv, sdesc_rows16(smem_u32(sSFV + vs * C::SF_ATOM)));
-        }
+        if constexpr (C::MX) tmem_cp_atom_w(sfv, sdesc_rows16(smem_u32(sSFV + vs * C::SF_ATOM)));
 #pragma unroll
         for (int k = 0; k < C::PV_MMAS; ++k) {
           const uint32_t a_t = tbase + C::T_P + b * 64 + k * (C::K_STEP * C::ESZ / 4);
@@ -750,7 +682,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (pc.j == pc.it.hi) mma_commit_w(&sm.o_full);
         ++u;
         pc.advance(args, n_work);
-        if (C::MX && pc.active) v_cur = mx_v_words<C>(args, pc.it, pc.j * kTileK, lane);
       }
       if (*abort_flag) {  // every MMA this warp issued has completed before TMEM goes away
         mma_commit_w(&sm.drain[1]);

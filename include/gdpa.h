@@ -108,10 +108,13 @@ typedef struct gdpa_shape {
 } gdpa_shape;
 
 /* Bytes of device workspace that gdpa_fwd (is_bwd = 0), gdpa_bwd
- * (is_bwd = 1) or gdpa_bwd with deterministic != 0 (is_bwd = 2) needs for
- * this problem; 0 for an invalid shape. The size depends only on the
- * arguments given here. The deterministic backward adds one fp32 dQ slice
- * [total_q, h_q, d_qk] per 128-key block of the longest key sequence. */
+ * (is_bwd = 1), gdpa_bwd with deterministic != 0 (is_bwd = 2) or
+ * gdpa_fwd_mxfp8 (is_bwd = 3) needs for this problem; 0 for an invalid
+ * shape. The size depends only on the arguments given here. The
+ * deterministic backward adds one fp32 dQ slice [total_q, h_q, d_qk] per
+ * 128-key block of the longest key sequence; gdpa_fwd_mxfp8 adds its scales
+ * rearranged into 512-byte tensor-memory copy atoms (about 4 d_qk / 32 + 1
+ * bytes per query or key row and head, rounded up to 128-row tiles). */
 size_t gdpa_workspace_bytes(const gdpa_shape* shape, int max_seqlen_q, int max_seqlen_k, int is_bwd);
 
 /* Forward. scale multiplies Q K^T before the activation (1/sqrt(d_qk) is the
@@ -146,8 +149,10 @@ int gdpa_fwd(const gdpa_shape* shape, const void* q, const void* k, const void* 
  *     Keys past a sequence's end inside its last block are ignored.
  * The MMAs apply the scales (tcgen05 kind::mxf8f6f4); P is quantised to e4m3
  * with scale 2^0. Head dims (128, 128) and (192, 128); every activation,
- * softmax included. The scale pointers must be 16-byte aligned. Other
- * arguments and errors as for gdpa_fwd (descale is not used). */
+ * softmax included. The scale pointers must be 16-byte aligned. The
+ * workspace is gdpa_workspace_bytes(shape, ..., 3) bytes: a first kernel
+ * rearranges the scales there into the atoms that the MMAs' scale copies
+ * read. Other arguments and errors as for gdpa_fwd (descale is not used). */
 int gdpa_fwd_mxfp8(const gdpa_shape* shape, const void* q, const void* k, const void* v,
                    const uint8_t* q_scale, const uint8_t* k_scale, const uint8_t* v_scale,
                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,

@@ -308,7 +308,9 @@ def main():
     lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=dev) if wl.act == "softmax" else None
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     shape = _lib.make_shape(q, k, v, wl.batch)
-    ws_f = torch.empty(_lib.gdpa_workspace_bytes(shape, mq, mk, False), dtype=torch.uint8, device=dev)
+    # the MXFP8 forward also stages its scale atoms in the workspace
+    ws_f = torch.empty(_lib.gdpa_workspace_bytes(shape, mq, mk, 3 if mxs is not None else 0), dtype=torch.uint8,
+                       device=dev)
     ws_b = torch.empty(_lib.gdpa_workspace_bytes(shape, mq, mk, True), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     a = (wl.act, wl.softmax_scale, wl.causal, wl.window)
@@ -509,11 +511,12 @@ def main():
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # per step: work list + forward kernel; backward: work list (which also clears the dQ
-        # accumulator), prep (softmax rowsum, or direct dQ's unwritten rows), main kernel and (unless
-        # dQ is written directly) the dQ convert
-        "gpu_launches": (2 + (0 if fwd_only else 2 + (1 if (wl.act == "softmax" or mk <= 128) else 0)
-                              + (1 if mk > 128 else 0))) * K,
+        # per step: work list + forward kernel (MXFP8: + the scale-atom staging); backward: work list
+        # (which also clears the dQ accumulator), prep (softmax rowsum, or direct dQ's unwritten rows),
+        # main kernel and (unless dQ is written directly) the dQ convert
+        "gpu_launches": (2 + (1 if mxs is not None else 0)
+                         + (0 if fwd_only else 2 + (1 if (wl.act == "softmax" or mk <= 128) else 0)
+                            + (1 if mk > 128 else 0))) * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -56,6 +56,14 @@ def test_workspace_bytes(lib):
     # backward holds an fp32 dQ accumulator
     assert bwd >= 256 * 4 * 128 * 4
     assert _lib.gdpa_workspace_bytes(_shape(h_q=3), 128, 128, False) == 0
+    # the MXFP8 forward adds its scale atoms (512 bytes each): per work item (at most
+    # total_q / 128 + batch + 1) and head, and per 32-key group and kv head, for q and k one
+    # atom per four 32-element blocks of d_qk, for v one
+    for d_qk, nqb in ((128, 1), (192, 2)):
+        sm = _shape(d_qk=d_qk, dtype=2)
+        r256 = lambda x: (x + 255) // 256 * 256
+        atoms = r256((256 // 128 + 2 + 1) * 4 * nqb * 512) + r256(8 * 2 * nqb * 512) + r256(8 * 2 * 512)
+        assert _lib.gdpa_workspace_bytes(sm, 128, 128, 3) - _lib.gdpa_workspace_bytes(sm, 128, 128, 0) == atoms
     # the deterministic backward adds one fp32 dQ slice per 128-key block of max_seqlen_k
     for max_k, nkv in ((128, 1), (129, 2), (300, 3)):
         det = _lib.gdpa_workspace_bytes(s, 128, max_k, 2)

@@ -194,10 +194,11 @@ __device__ __forceinline__ int4 item_blocks(const Problem& pb, int mode, int blk
 }
 
 // Cost bucket of a sequence: its heaviest block's cost.
-__device__ __forceinline__ int seq_bucket(const Problem& pb, int mode, int nblk, int lq, int lk) {
+// Called by a whole warp for one sequence: its items are shared out over the lanes.
+__device__ __forceinline__ int seq_bucket_warp(const Problem& pb, int mode, int nblk, int lq, int lk, int lane) {
   int c = 0;
-  for (int blk = 0; blk < nblk; ++blk) c = max(c, item_blocks(pb, mode, blk, lq, lk).w);
-  return min(c, kBuckets - 1);
+  for (int blk = lane; blk < nblk; blk += 32) c = max(c, item_blocks(pb, mode, blk, lq, lk).w);
+  return min(__reduce_max_sync(0xffffffffu, c), kBuckets - 1);
 }
 
 // Block 0 builds the list; any further blocks zero `clear` (n4 float4s, the
@@ -216,13 +217,17 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
   for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int rows = mode == 0 ? kFwdItemRows : kTileK;
-  for (int b = threadIdx.x; b < pb.batch; b += blockDim.x) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // one warp per sequence (a sequence's items can number in the hundreds)
+  for (int b = wid; b < pb.batch; b += nwarps) {
     int qs, lq, ks, lk;
     seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
     seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
     const int len = mode == 0 ? lq : lk;
     const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
-    if (nblk > 0) atomicAdd(&hist[seq_bucket(pb, mode, nblk, lq, lk)], nblk);
+    if (nblk == 0) continue;
+    const int c = seq_bucket_warp(pb, mode, nblk, lq, lk, lane);
+    if (lane == 0) atomicAdd(&hist[c], nblk);
   }
   __syncthreads();
   // exclusive prefix over the buckets, heaviest first: each of the 1024
@@ -232,7 +237,6 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
   __shared__ int warp_sum[32];
   const int c0 = kBuckets - 1 - 2 * static_cast<int>(threadIdx.x), c1 = c0 - 1;
   const int h0 = hist[c0], h1 = hist[c1];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int incl = h0 + h1;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -259,15 +263,18 @@ __global__ void __launch_bounds__(1024) build_worklist(Problem pb, int mode, Wor
     wl->count = run < cap ? run : cap;
   }
   __syncthreads();
-  for (int b = threadIdx.x; b < pb.batch; b += blockDim.x) {
+  for (int b = wid; b < pb.batch; b += nwarps) {
     int qs, lq, ks, lk;
     seq_bounds(pb.cu_q, b, pb.max_q, qs, lq);
     seq_bounds(pb.cu_k, b, pb.max_k, ks, lk);
     const int len = mode == 0 ? lq : lk;
     const int nblk = len > 0 ? (len + rows - 1) / rows : 0;
     if (nblk == 0) continue;
-    const int base = atomicAdd(&hist[seq_bucket(pb, mode, nblk, lq, lk)], nblk);  // the sequence's slots
-    for (int i = 0; i < nblk; ++i) {
+    const int c = seq_bucket_warp(pb, mode, nblk, lq, lk, lane);
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&hist[c], nblk);  // the sequence's slots
+    base = __shfl_sync(0xffffffffu, base, 0);
+    for (int i = lane; i < nblk; i += 32) {
       // causal costs grow with the query tile and shrink with the key block: heaviest first
       const int blk = mode == 0 ? nblk - 1 - i : i;
       const int p = base + i;

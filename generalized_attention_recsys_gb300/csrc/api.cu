@@ -148,6 +148,10 @@ size_t dq_part_bytes(const gdpa_shape* s, int max_k) {
   return nkv * static_cast<size_t>(s->total_q) * s->h_q * s->d_qk * sizeof(float);
 }
 
+// Sequences stay below 2^30 tokens, so that mask arithmetic (a position plus
+// a window) cannot overflow an int; a longer window selects the same keys.
+constexpr int kMaxSeqLen = 1 << 30;
+
 int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int window) {
   (void)causal;
   (void)window;
@@ -161,6 +165,7 @@ int validate(const gdpa_shape* s, int max_q, int max_k, int act, int causal, int
   if (!ok_dims) return GDPA_ERR_UNSUPPORTED;
   if (static_cast<long long>(s->total_q) * s->h_q * (s->d_qk > s->d_v ? s->d_qk : s->d_v) >= (1ll << 40))
     return GDPA_ERR_UNSUPPORTED;
+  if (max_q >= kMaxSeqLen || max_k >= kMaxSeqLen) return GDPA_ERR_UNSUPPORTED;
   return GDPA_OK;
 }
 
@@ -487,7 +492,7 @@ Problem make_problem(const gdpa_shape* s, const int32_t* cu_q, const int32_t* cu
   pb.cu_q = cu_q;
   pb.cu_k = cu_k;
   pb.causal = causal ? 1 : 0;
-  pb.window = window > 0 ? window : 0;
+  pb.window = window > 0 ? (window < kMaxSeqLen ? window : kMaxSeqLen) : 0;
   return pb;
 }
 

@@ -40,8 +40,10 @@
  * Errors. Problems visible on the host are returned before any launch:
  * GDPA_ERR_INVALID (null or misaligned pointer, negative size, h_q % h_kv,
  * bad enum), GDPA_ERR_UNSUPPORTED (head dims other than (64,64), (96,96),
- * (128,128), (192,128); FP8 backward), GDPA_ERR_WORKSPACE (too small),
- * GDPA_ERR_CUDA (a launch or tensor-map encode failed). Every device-side wait
+ * (128,128), (192,128); FP8 backward; max_seqlen of 2^30 or more),
+ * GDPA_ERR_WORKSPACE (too small),
+ * GDPA_ERR_CUDA (a launch or tensor-map encode failed). A window of 2^30 or
+ * more is the same as none. Every device-side wait
  * is bounded; a wait that gives up records GDPA_ERR_TIMEOUT in a per-device
  * status word that gdpa_get_status() returns. cu_seqlens consistency
  * (monotone, lengths <= max_seqlen, cu[batch] = total) is a caller

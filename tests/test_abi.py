@@ -56,6 +56,10 @@ def test_workspace_bytes(lib):
     # backward holds an fp32 dQ accumulator
     assert bwd >= 256 * 4 * 128 * 4
     assert _lib.gdpa_workspace_bytes(_shape(h_q=3), 128, 128, False) == 0
+    # sequences of 2^30 tokens or more are refused (mask arithmetic stays within int)
+    assert _lib.gdpa_workspace_bytes(s, 1 << 30, 128, False) == 0
+    assert _lib.gdpa_workspace_bytes(s, 128, 1 << 30, False) == 0
+    assert _lib.gdpa_workspace_bytes(s, (1 << 30) - 1, 128, False) > 0
     # the MXFP8 forward adds its scale atoms (512 bytes each): per work item (at most
     # total_q / 128 + batch + 1) and head, and per 32-key group and kv head, for q and k one
     # atom per four 32-element blocks of d_qk, for v one

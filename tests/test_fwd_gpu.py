@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from generalized_attention_recsys_gb300 import inputs
-from gpu_util import FP8_TOL, FWD_TOL, assert_close, ref_fwd, run_fwd
+from gpu_util import FP8_TOL, FWD_TOL, assert_close, ref_fwd, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +42,24 @@ def test_masks_and_heads(causal, window, h_kv):
     out, _ = run_fwd(inp)
     ref, _ = ref_fwd(inp)
     assert_close(out, ref, FWD_TOL, f"out causal={causal} window={window} h_kv={h_kv}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_window_beyond_any_length_is_no_window(causal):
+    # a window at the top of the int range must select the same keys as no window
+    # (the library clamps it below 2^30, so the mask arithmetic cannot overflow)
+    lq, lk = [100, 257, 3, 130], [300, 257, 9, 64]
+    wide = inputs.custom(4, 2, 1, 128, 128, lq, lk, "gelu", causal=causal, window=2**31 - 1, seed=7)
+    none = inputs.custom(4, 2, 1, 128, 128, lq, lk, "gelu", causal=causal, window=-1, seed=7)
+    out_wide, _ = run_fwd(wide)
+    out_none, _ = run_fwd(none)
+    assert torch.equal(out_wide, out_none)
+    ref, _ = ref_fwd(none)
+    assert_close(out_wide, ref, FWD_TOL, f"out causal={causal} window=2^31-1")
+    dq_w, dk_w, dv_w = run_bwd(wide)
+    dq_n, dk_n, dv_n = run_bwd(none)
+    assert torch.equal(dk_w, dk_n) and torch.equal(dv_w, dv_n)
+    assert torch.allclose(dq_w.float(), dq_n.float(), rtol=0, atol=1e-2 * dq_n.float().abs().max().item())
 
 
 @pytest.mark.parametrize("dims", [(64, 64), (96, 96), (192, 128)])

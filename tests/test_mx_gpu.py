@@ -4,8 +4,9 @@ the keys), applied by the block-scaled MMAs. Checked against the float64
 oracle on the dequantised values at the FP8 tolerance: jagged query lengths
 (empty, one row, ragged tails), key lengths that keep every key sequence on
 a 32-key block boundary (the last sequence ragged), GQA/MQA, causal and
-sliding-window masks, both supported head-dim pairs, head counts above
-the 16 heads that the scale rearrangement stages at a time, and several
+sliding-window masks, both supported head-dim pairs, head counts up to
+64 (past what one shared-memory tile row of the scale rearrangement holds
+at d_qk = 192, so it takes the heads in two chunks), and several
 activations, softmax included. A key sequence that starts off a block is
 reported through the device status word."""
 
@@ -29,8 +30,9 @@ LK = [224, 128, 32, 448, 0, 320, 101]  # multiples of 32 but the last: every seq
     ((192, 128), 4, 4, "identity", False, 60),
     ((192, 128), 4, 1, "silu", False, -1),
     ((192, 128), 2, 2, "softmax", False, -1),
-    ((128, 128), 24, 3, "fast_gelu", True, -1),   # more q heads than one scale-staging tile holds
-    ((192, 128), 36, 18, "gelu", False, 200),     # likewise for k heads
+    ((128, 128), 24, 3, "fast_gelu", True, -1),   # GQA 8 over an odd number of kv heads
+    ((192, 128), 36, 18, "gelu", False, 200),     # many kv heads
+    ((192, 128), 64, 1, "relu", True, -1),        # q heads past one staging tile row (two head chunks)
 ])
 def test_mxfp8_forward_matches_oracle(dims, h_q, h_kv, act, causal, window):
     inp = inputs.custom(len(LQ), h_q, h_kv, dims[0], dims[1], LQ, LK, act, causal=causal, window=window,
